@@ -1,0 +1,244 @@
+/*
+ * dfv.h -- C ABI of libdfv, the greedy DDTree tree-verify step on GB300
+ * (sm_103a).
+ *
+ * The step (as described on "Luce DFlash: Qwen3.6-27B aiming for up to 2x
+ * throughput on a single RTX 3090", ai-navigate-news (ja), feature list:
+ * DDTree tree-verify, block size 16, default budget 22, greedy
+ * verification, Q4_0 KV cache, 2048-token sliding-window flash attention at
+ * decode; and "We got 207 tok/s with Qwen3.5-27B on an RTX 3090", nowletus,
+ * DFlash section) has four parts, one entry point each:
+ *
+ *   dfv_tree_verify_attn  tree-masked attention of the N = budget + 1 draft
+ *                         nodes over the Q4_0 cache (dequantised on the fly)
+ *   dfv_greedy_accept     per-node vocabulary argmax + greedy tree walk
+ *   dfv_kv_commit         Q4_0 re-quantisation of the accepted K/V rows into
+ *                         the cache; rejected rows are never written
+ *   dfv_verify_step       the three above, in order, on one stream
+ *
+ * plus dfv_kv_quantize_rows, the same Q4_0 quantiser used to fill a cache
+ * from float rows (prefill).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor pointers are DEVICE pointers owned by the caller. The library
+ *   allocates no memory. Scratch memory ("workspace") is passed in by the
+ *   caller; its size comes from the matching *_workspace_bytes() query.
+ * - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *   NULL = the legacy default stream). No entry point synchronises.
+ * - The return value reports only what the host can check before launch:
+ *   DFV_ERR_INVALID (null pointer, size out of range, misaligned pointer),
+ *   DFV_ERR_UNSUPPORTED (valid but unsupported combination),
+ *   DFV_ERR_WORKSPACE (workspace too small), DFV_ERR_CUDA (launch failed;
+ *   the CUDA error is left for the caller to read). Nothing is launched when
+ *   an error is returned.
+ * - Problems only the device can see are OR-ed into `*status` (a device
+ *   uint32, may be NULL): DFV_DEV_* bits below. The caller clears it.
+ * - The committed length lives in device memory (`ctx_len`), so a loop of
+ *   steps never needs a host round trip.
+ * - bf16 / f16 / f32 are IEEE types in little-endian device memory.
+ *
+ * Data layouts
+ * ------------
+ * KV cache (K and V each): Q4_0 blocks, [n_kv_heads][cache_capacity][D/32],
+ *   one block = 18 bytes: fp16 scale d, then 16 bytes of 4-bit codes (byte j
+ *   = code j in the low nibble, code j+16 in the high nibble); the block's
+ *   values are (code - 8) * d. Row (head h, position p) starts at byte
+ *   (h * cache_capacity + p) * (D / 32) * 18. Base pointer 16-byte aligned.
+ * Tree nodes: node 0 is the root; parent[i] in [0, i) for i >= 1 (parent[0]
+ *   is ignored). Committed key j sits at position j, node i at position
+ *   ctx_len + depth(i).
+ * Visibility: node i sees committed key j iff j < ctx_len and
+ *   (window == 0 or ctx_len + depth(i) - j < window), and tree node t iff t
+ *   is i or an ancestor of i. Query head h uses KV head h / (Hq / Hkv).
+ */
+#ifndef DFV_H
+#define DFV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void* dfv_stream_t; /* a cudaStream_t */
+
+typedef enum dfv_status {
+  DFV_OK = 0,
+  DFV_ERR_INVALID = 1,
+  DFV_ERR_UNSUPPORTED = 2,
+  DFV_ERR_WORKSPACE = 3,
+  DFV_ERR_CUDA = 4
+} dfv_status;
+
+/* Device-detected problems, OR-ed into *status. */
+#define DFV_DEV_BAD_TREE 0x1u  /* parent[i] outside [0, i): treated as 0      */
+#define DFV_DEV_DEPTH 0x2u     /* a node deeper than max_depth (still run)    */
+#define DFV_DEV_CAPACITY 0x4u  /* ctx_len + accept_len > capacity: no write   */
+#define DFV_DEV_CTX 0x8u       /* *ctx_len outside [0, capacity]: no work     */
+#define DFV_DEV_BAD_PATH 0x10u /* path entry outside [0, n_nodes): no write   */
+#define DFV_DEV_TIMEOUT 0x20u  /* a bounded wait gave up; outputs undefined   */
+
+#define DFV_KV_Q4_0 2 /* the only KV format ("Q4_0", 18-byte blocks) */
+
+#define DFV_DTYPE_F32 0
+#define DFV_DTYPE_BF16 1
+
+#define DFV_MAX_NODES 65 /* budget <= 64 */
+
+/* Human-readable name of a status code (static string). */
+const char* dfv_status_string(dfv_status s);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int dfv_version(void);
+
+/* ------------------------------------------------------------------------
+ * dfv_tree_verify_attn -- tree-masked attention over a Q4_0 cache.
+ *
+ * Passage: "Luce DFlash: Qwen3.6-27B ..." (ai-navigate-news, ja), feature
+ * list -- DDTree tree-verify (block 16, budget 22) and sliding-window flash
+ * attention at decode (default window 2048) over the Q4_0 KV cache.
+ *
+ * out[i][h][:] = sum_k softmax_k(scale * q[i][h] . key_k) * value_k over the
+ * keys visible to node i (see "Visibility" above); committed keys/values are
+ * the cache's Q4_0 rows dequantised, tree keys/values are tree_k / tree_v.
+ *
+ *   n_nodes        N = budget + 1, 1..DFV_MAX_NODES
+ *   max_depth      bound on tree depth (block size); deeper -> DFV_DEV_DEPTH
+ *   n_q_heads      Hq;  n_kv_heads Hkv; Hq % Hkv == 0, Hq <= 256
+ *   head_dim       D in {64, 128, 256}
+ *   window         sliding window in positions, 0 = none
+ *   kv_format      DFV_KV_Q4_0
+ *   cache_capacity positions per head in the cache
+ *   ctx_len        device int32[1], committed length C (read only)
+ *   k_cache,v_cache  device Q4_0 cache (layout above), read only
+ *   q              device bf16 [N][Hq][D]
+ *   tree_k,tree_v  device bf16 [N][Hkv][D], the tree nodes' own K/V rows
+ *   parent         device int32 [N]
+ *   scale          softmax scale; <= 0 means 1/sqrt(D)
+ *   out            device f32 [N][Hq][D]
+ *   lse            device f32 [N][Hq] (natural-log log-sum-exp), may be NULL
+ *   workspace      device scratch, >= dfv_tree_verify_attn_workspace_bytes()
+ *                  bytes, 256-byte aligned; no initialisation needed
+ *   status         device uint32[1] or NULL
+ *
+ * Value range: |q|, |tree_k|, |tree_v| and the cache values must stay within
+ * the fp16 range (the tensor-core operands are fp16).
+ * ---------------------------------------------------------------------- */
+size_t dfv_tree_verify_attn_workspace_bytes(int n_nodes, int n_q_heads, int n_kv_heads,
+                                            int head_dim, int window, int cache_capacity);
+
+dfv_status dfv_tree_verify_attn(int n_nodes, int max_depth, int n_q_heads, int n_kv_heads,
+                                int head_dim, int window, int kv_format, int cache_capacity,
+                                const int32_t* ctx_len, const void* k_cache, const void* v_cache,
+                                const void* q, const void* tree_k, const void* tree_v,
+                                const int32_t* parent, float scale, float* out, float* lse,
+                                void* workspace, size_t workspace_bytes, uint32_t* status,
+                                dfv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * dfv_greedy_accept -- per-node argmax and greedy tree walk.
+ *
+ * Passage: "Luce DFlash: Qwen3.6-27B ..." (ai-navigate-news, ja), feature
+ * list (greedy verification) and constraints paragraph (greedy verify only).
+ *
+ * argmax[i] = the lowest index of the maximum of logits[i][:] (-0.0 equals
+ * +0.0; logits must hold no NaN). The walk starts at the root and, while
+ * some child c of the last accepted node has tokens[c] == argmax[last],
+ * accepts the lowest-index such child.
+ *
+ *   n_nodes       N, 1..DFV_MAX_NODES;  vocab V >= 1
+ *   logits_dtype  DFV_DTYPE_F32 or DFV_DTYPE_BF16; logits device [N][V]
+ *   parent        device int32 [N];  tokens device int32 [N] (draft tokens;
+ *                 tokens[0] is not read)
+ *   argmax        device int32 [N]                       (out)
+ *   accept_len    device int32 [1], L = accepted nodes incl. root, >= 1 (out)
+ *   path          device int32 [N], accepted node ids root first; entries
+ *                 from L on are set to -1                (out)
+ *   out_tokens    device int32 [N], tokens[path[1..L-1]] then the bonus
+ *                 argmax[path[L-1]]; entries from L on are -1 (out)
+ *   workspace     >= dfv_greedy_accept_workspace_bytes(); must be zeroed
+ *                 once before its first use (dfv_workspace_clear); every
+ *                 call leaves it zeroed again
+ *   status        device uint32[1] or NULL
+ * ---------------------------------------------------------------------- */
+size_t dfv_greedy_accept_workspace_bytes(int n_nodes, int vocab);
+
+dfv_status dfv_greedy_accept(int n_nodes, int vocab, int logits_dtype, const void* logits,
+                             const int32_t* parent, const int32_t* tokens, int32_t* argmax,
+                             int32_t* accept_len, int32_t* path, int32_t* out_tokens,
+                             void* workspace, size_t workspace_bytes, uint32_t* status,
+                             dfv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * dfv_kv_commit -- commit the accepted rows, roll back the rest.
+ *
+ * Passage: "We got 207 tok/s with Qwen3.5-27B on an RTX 3090" (nowletus),
+ * "What we ported and tuned": Q4_0 KV cache; "Luce DFlash ..." feature list:
+ * tree-verify over that cache.
+ *
+ * For k < L = *accept_len and every KV head h, quantises tree_k[path[k]][h]
+ * (and tree_v) to Q4_0 and writes it at cache position C + k, C = *ctx_len;
+ * then *ctx_len = C + L. Positions >= C + L are not touched (rejected nodes
+ * are never written). If C + L > cache_capacity, or a path entry is outside
+ * [0, n_nodes), nothing is written, *ctx_len is unchanged and a DFV_DEV_*
+ * bit is set.
+ *
+ * Q4_0 rule per 32-value block (binary32, round-to-nearest-even, no fused
+ * multiply-add): m = first element of largest magnitude, d = m / -8,
+ * id = d != 0 ? 1 / d : 0, code = min(15, trunc((x * id) + 8.5)), scale
+ * stored as fp16(d).
+ *
+ *   n_nodes       N (bounds the path entries and L)
+ *   ctx_len       device int32[1], read and advanced
+ *   accept_len    device int32[1];  path device int32 [>= L]
+ *   tree_k/v      device bf16 [N][Hkv][D]
+ *   k_cache/v_cache  device Q4_0 cache, written at rows [C, C + L)
+ * ---------------------------------------------------------------------- */
+dfv_status dfv_kv_commit(int n_nodes, int n_kv_heads, int head_dim, int kv_format,
+                         int cache_capacity, int32_t* ctx_len, const int32_t* accept_len,
+                         const int32_t* path, const void* tree_k, const void* tree_v,
+                         void* k_cache, void* v_cache, uint32_t* status, dfv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * dfv_kv_quantize_rows -- fill cache rows [pos0, pos0 + n_rows) of every KV
+ * head from float rows, with the Q4_0 rule of dfv_kv_commit (prefill).
+ *
+ *   src        device f32 or bf16 (src_dtype); element (row r, head h, dim
+ *              c) at src[r * stride_row + h * stride_head + c] (elements)
+ *   cache      device Q4_0 cache, written; ctx_len is not touched
+ * ---------------------------------------------------------------------- */
+dfv_status dfv_kv_quantize_rows(int n_kv_heads, int head_dim, int kv_format, int cache_capacity,
+                                int pos0, int n_rows, const void* src, int src_dtype,
+                                int64_t stride_row, int64_t stride_head, void* cache,
+                                dfv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * dfv_verify_step -- one whole greedy tree-verify step: attention, argmax +
+ * walk, commit, in that order on `stream`. Arguments as in the three entry
+ * points above; `workspace` holds both scratch areas
+ * (dfv_verify_step_workspace_bytes) and must be zeroed once before its
+ * first use.
+ * ---------------------------------------------------------------------- */
+size_t dfv_verify_step_workspace_bytes(int n_nodes, int n_q_heads, int n_kv_heads, int head_dim,
+                                       int window, int cache_capacity, int vocab);
+
+dfv_status dfv_verify_step(int n_nodes, int max_depth, int n_q_heads, int n_kv_heads,
+                           int head_dim, int window, int kv_format, int cache_capacity,
+                           int vocab, int logits_dtype, int32_t* ctx_len, void* k_cache,
+                           void* v_cache, const void* q, const void* tree_k, const void* tree_v,
+                           const int32_t* parent, const int32_t* tokens, const void* logits,
+                           float scale, float* out, float* lse, int32_t* argmax,
+                           int32_t* accept_len, int32_t* path, int32_t* out_tokens,
+                           void* workspace, size_t workspace_bytes, uint32_t* status,
+                           dfv_stream_t stream);
+
+/* Zero `bytes` of a caller-owned workspace on `stream` (no allocation). */
+dfv_status dfv_workspace_clear(void* workspace, size_t bytes, dfv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFV_H */

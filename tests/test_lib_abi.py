@@ -1,0 +1,58 @@
+"""The C-ABI library builds, loads and exports every declared symbol (no GPU
+compute)."""
+
+import os
+import re
+
+import pytest
+
+from tree_verify_attention_gb300 import _lib
+from tree_verify_attention_gb300 import build as B
+
+HEADER = os.path.join(B.ROOT, "include", "dfv.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dfv_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return _lib.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_binding_table_matches_header():
+    assert set(_lib.SIGNATURES) == set(declared_functions())
+
+
+def test_status_strings_and_version(lib):
+    assert lib.dfv_status_string(0) == b"ok"
+    assert lib.dfv_status_string(3) == b"workspace too small"
+    assert lib.dfv_version() >= 100
+
+
+def test_host_side_rejections(lib):
+    # invalid shapes are rejected before any device call
+    assert lib.dfv_tree_verify_attn_workspace_bytes(0, 24, 4, 256, 2048, 100) == 0
+    assert lib.dfv_tree_verify_attn_workspace_bytes(66, 24, 4, 256, 2048, 100) == 0
+    assert lib.dfv_tree_verify_attn_workspace_bytes(23, 24, 5, 256, 2048, 100) == 0
+    assert lib.dfv_tree_verify_attn_workspace_bytes(23, 24, 4, 96, 2048, 100) == 0
+    assert lib.dfv_greedy_accept_workspace_bytes(0, 10) == 0
+    st = lib.dfv_greedy_accept(23, 100, 0, None, None, None, None, None, None, None, None, 0,
+                               None, None)
+    assert st == 1  # DFV_ERR_INVALID
+    st = lib.dfv_kv_commit(23, 4, 256, 3, 100, None, None, None, None, None, None, None, None,
+                           None)
+    assert st == 2  # DFV_ERR_UNSUPPORTED (format)
+    st = lib.dfv_kv_quantize_rows(4, 96, 2, 100, 0, 1, None, 0, 1, 1, None, None)
+    assert st == 2

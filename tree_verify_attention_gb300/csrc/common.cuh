@@ -1,0 +1,173 @@
+// Shared device helpers of libdfv (sm_103a): status reporting, bounded
+// mbarrier waits, 1-D bulk copies (TMA engine), ldmatrix and mma.sync
+// wrappers. Inline PTX is hand-written here.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "dfv.h"
+
+namespace dfv {
+
+constexpr int kMaxNodes = DFV_MAX_NODES;
+constexpr int kMaskWords = (kMaxNodes + 31) / 32;   // 3
+// Bound on polling iterations of any wait (each try_wait may also suspend
+// in hardware for a while); reaching it sets DFV_DEV_TIMEOUT.
+constexpr uint32_t kWaitLimit = 1u << 26;
+
+__device__ __forceinline__ void report(uint32_t* status, uint32_t bits) {
+  if (status != nullptr) atomicOr(status, bits);
+}
+
+// ---------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// One poll of phase `parity`; true once that phase has completed.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait; false if the limit was reached.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  for (uint32_t it = 0; it < kWaitLimit; ++it)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// 1-D bulk copy global -> shared through the TMA engine, completing
+// `bytes` of transaction count on `bar`. dst, src 16-byte aligned; bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ---------------------------------------------------------------- tensor core (legacy path)
+
+__device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
+                                        const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
+                                          const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_u32(p)));
+}
+
+// D += A * B, m16n8k16, f16 inputs, f32 accumulators.
+__device__ __forceinline__ void mma_f16(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ---------------------------------------------------------------- Q4_0
+
+// Dequantise the 16 code bytes + fp16 scale of one Q4_0 block into 32 fp16
+// values (q - 8) * d: the integer (q - 8) is exact in fp16, the product is
+// rounded once to nearest. `codes` is 2-byte aligned.
+__device__ __forceinline__ void q4_0_block_to_half(const uint16_t* codes, __half d,
+                                                   __half* out_lo16, __half* out_hi16) {
+  const __half2 d2 = __halves2half2(d, d);
+  const __half2 bias = __float2half2_rn(1032.0f);  // 1024 + 8
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t u = codes[k];                   // bytes 2k (low), 2k+1 (high)
+    // 0x6400 | n is the fp16 value 1024 + n for n in [0, 15]
+    const uint32_t lo = 0x64006400u | (u & 0x000Fu) | ((u & 0x0F00u) << 8);
+    const uint32_t hi = 0x64006400u | ((u >> 4) & 0x000Fu) | ((u & 0xF000u) << 4);
+    __half2 vlo = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&lo), bias), d2);
+    __half2 vhi = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&hi), bias), d2);
+    *reinterpret_cast<__half2*>(out_lo16 + 2 * k) = vlo;
+    *reinterpret_cast<__half2*>(out_hi16 + 2 * k) = vhi;
+  }
+}
+
+// Quantise 32 float values to one Q4_0 block with the binary32 rule:
+// m = first element of largest magnitude, d = m / -8, id = 1/d (0 if d = 0),
+// code = min(15, trunc(RN(RN(x * id) + 8.5))); scale stored as fp16 RN(d).
+__device__ __forceinline__ void q4_0_quantize_block(const float* x, uint8_t* blk) {
+  float amax = -1.0f, m = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    const float a = fabsf(x[k]);
+    if (a > amax) { amax = a; m = x[k]; }
+  }
+  const float d = __fdiv_rn(m, -8.0f);
+  const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+  uint8_t q[32];
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    const float t = __fadd_rn(__fmul_rn(x[k], id), 8.5f);
+    const int c = __float2int_rz(t);
+    q[k] = static_cast<uint8_t>(c < 15 ? c : 15);
+  }
+  const __half dh = __float2half_rn(d);
+  uint16_t* w = reinterpret_cast<uint16_t*>(blk);   // blocks are 2-byte aligned
+  w[0] = __half_as_ushort(dh);
+#pragma unroll
+  for (int j = 0; j < 16; j += 2) {
+    const uint32_t b0 = q[j] | (q[j + 16] << 4);
+    const uint32_t b1 = q[j + 1] | (q[j + 17] << 4);
+    w[1 + j / 2] = static_cast<uint16_t>(b0 | (b1 << 8));
+  }
+}
+
+// ---------------------------------------------------------------- host helpers
+
+int sm_count();   // SMs of the current device (cached per device)
+
+inline bool aligned(const void* p, size_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+}  // namespace dfv
