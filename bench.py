@@ -1,0 +1,535 @@
+#!/usr/bin/env python3
+"""Benchmark of the greedy tree-verify step on one GB300 (or N replicas).
+
+Workload: context 61440 tokens of Q4_0 K/V, 2048-token sliding window,
+24 query / 4 KV heads, head_dim 256, budget 22 (23 tree nodes, random tree
+of depth <= 16 with a planted accepted path), vocabulary 151936 bf16
+logits; every step is verify + commit, and each step's commit precedes the
+next step's attention (strictly serial steps, one stream, one CUDA graph).
+
+Inputs larger than L2: 64 distinct step inputs (7.4 MB each) and 64 KV-cache
+replicas (one per step modulo 64, standing in for a model's attention
+layers) are cycled, so every step reads its KV window and logits from HBM.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Prints one JSON line (rank 0).
+"""
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verify steps/s @ctx 60K, budget 22; KV+logits HBM GB/s and % of GB300 peak"
+UNIT = "steps/s"
+WORKLOAD = "long_ctx61440_w2048_b22"
+POOL = 64        # distinct step inputs
+REPLICAS = 64    # KV-cache replicas
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["dfv", "reference"], default="dfv")
+    ap.add_argument("--e2e-steps", type=int, default=256)
+    ap.add_argument("--probe-steps", type=int, default=256)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pool", type=int, default=POOL, help="distinct step inputs")
+    ap.add_argument("--replicas", type=int, default=REPLICAS, help="KV-cache replicas")
+    ap.add_argument("--cpu-child", action="store_true", help=argparse.SUPPRESS)
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------- multi-process plumbing
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(x, world, device=None):
+    """Max of a host float over all ranks (identity when world == 1)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(local_elapsed_s, steps, world, device=None):
+    """Whole-job throughput: all ranks' steps over the slowest rank's time."""
+    t = max_over_ranks(local_elapsed_s, world, device)
+    return world * steps / t, t
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id=None, path=None):
+        self.gpu_id, self.path, self.proc = gpu_id, path, None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.gpu_id is not None:
+            cmd += ["-i", str(self.gpu_id)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 8]
+        if self.path:
+            with open(self.path, "w") as f:
+                f.write(out)
+        sm, mx, pw, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                pw.append(float(r[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip() == "Active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def cpu_oracle_child(seconds, max_steps):
+    """Time the oracle's whole verify step on a bounded sample of the
+    workload (runs in a single-threaded child process)."""
+    import numpy as np
+    import oracle
+    from tree_verify_attention_gb300 import workload as W
+    cfg = W.LONG_WINDOW
+    kf, vf = W.make_context(cfg)
+    cap = cfg.ctx_len + 64 * cfg.n_nodes
+    kc = np.zeros((cfg.n_kv_heads, cap, cfg.head_dim // 32, 18), np.uint8)
+    vc = np.zeros_like(kc)
+    kc[:, :cfg.ctx_len] = oracle.q4_0.quantize_rows(kf)
+    vc[:, :cfg.ctx_len] = oracle.q4_0.quantize_rows(vf)
+    del kf, vf
+    inputs = [W.make_step(cfg, i) for i in range(4)]
+    ctx = cfg.ctx_len
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        s = inputs[n % len(inputs)]
+        res = oracle.step.verify_step(kc, vc, ctx, cfg.window, W.bf16_bits_to_f32(s.q),
+                                      W.bf16_bits_to_f32(s.k_tree), W.bf16_bits_to_f32(s.v_tree),
+                                      s.parent, s.tokens, W.bf16_bits_to_f32(s.logits))
+        ctx = res["ctx_len"]
+        n += 1
+        el = time.perf_counter() - t0
+        if n >= max_steps or (el >= seconds and n >= 2):
+            break
+    print(json.dumps({"steps": n, "seconds": el, "value": n / el}))
+
+
+def run_cpu_oracle(seconds, max_steps=10 ** 9):
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-child",
+                        "--cpu-seconds", str(seconds), "--steps", str(max_steps)],
+                       env=env, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("CPU oracle timing failed:\n" + r.stderr[-2000:])
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    res["sample"] = (f"oracle verify_step (fp64 tree attention over the 2047-key window, "
+                     f"23 x 151936 argmax, greedy walk, Q4_0 commit) at ctx 61440: "
+                     f"{res['steps']} consecutive steps, {res['seconds']:.1f} s, one thread")
+    return res
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    res = run_cpu_oracle(seconds=min(60.0, args.cpu_seconds * 4), max_steps=args.steps)
+    cpu = {"value": res["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
+           "sample": res["sample"]}
+    line = {"impl": "reference", "metric": METRIC, "value": res["value"], "unit": UNIT,
+            "n_gpus": args.gpus, "steps": res["steps"], "warmup": 0,
+            "ms_per_step": 1000.0 * res["seconds"] / res["steps"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "ctx": 61440, "window": 2048, "budget": 22,
+                       "heads": "24/4", "head_dim": 256, "vocab": 151936},
+            "cpu_baseline": cpu,
+            "e2e": {"value": res["value"], "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- the GPU arm
+
+class CacheView:
+    """A replica's K/V byte tensors and committed length (views into the
+    replica pool), shaped like api.Q4Cache."""
+
+    def __init__(self, k, v, ctx_len, n_kv_heads, head_dim, capacity):
+        self.k, self.v, self.ctx_len = k, v, ctx_len
+        self.n_kv_heads, self.head_dim, self.capacity = n_kv_heads, head_dim, capacity
+
+
+def algorithmic_per_step(cfg, parents):
+    """KV bytes, logits bytes and attention flops one step must move / do,
+    averaged over the step inputs (the flops depend on the tree only
+    through the window bound, so they are equal for every input here)."""
+    import numpy as np
+    D, hkv, hq, N, W_, C = (cfg.head_dim, cfg.n_kv_heads, cfg.n_q_heads, cfg.n_nodes,
+                            cfg.window, cfg.ctx_len)
+    row = D // 32 * 18
+    kv_rows = min(W_ - 1, C) if W_ > 0 else C
+    kv_bytes = kv_rows * row * 2 * hkv
+    logits_bytes = N * cfg.vocab * 2
+    flops = []
+    for parent in parents:
+        depth = np.zeros(N, dtype=np.int64)
+        for i in range(1, N):
+            depth[i] = depth[parent[i]] + 1
+        vis = 0
+        for i in range(N):
+            lo = max(0, C + depth[i] - W_ + 1) if W_ > 0 else 0
+            vis += max(0, C - lo) + depth[i] + 1
+        flops.append(4.0 * vis * hq * D)
+    return kv_bytes, logits_bytes, float(np.mean(flops))
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from tree_verify_attention_gb300 import api, build
+    from tree_verify_attention_gb300 import workload as W
+    build.build()
+    cfg = W.LONG_WINDOW
+    N, hq, hkv, D, Wn, V, C = (cfg.n_nodes, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim,
+                               cfg.window, cfg.vocab, cfg.ctx_len)
+    K, Wu = args.steps, max(3, args.warmup)
+    per_phase = max(K, Wu, args.e2e_steps, args.probe_steps)
+    n_pool, n_rep = args.pool, args.replicas
+    cap = C + (math.ceil(per_phase / n_rep) + 2) * N
+    row = D // 32 * 18
+
+    # ---- inputs: step pool (independent per rank) and cache replicas
+    seed_off = 1000 * rank
+    steps_np = [W.make_step(cfg, seed_off + i) for i in range(n_pool)]
+
+    def bf(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
+
+    q_all = torch.stack([bf(s.q) for s in steps_np]).to(dev)
+    tk_all = torch.stack([bf(s.k_tree) for s in steps_np]).to(dev)
+    tv_all = torch.stack([bf(s.v_tree) for s in steps_np]).to(dev)
+    par_all = torch.stack([torch.from_numpy(s.parent) for s in steps_np]).to(dev)
+    tok_all = torch.stack([torch.from_numpy(s.tokens) for s in steps_np]).to(dev)
+    lg_all = torch.stack([bf(s.logits) for s in steps_np]).to(dev)
+
+    kf, vf = W.make_context(cfg, seed=cfg.seed + rank)
+    base = api.Q4Cache(hkv, D, cap, device=dev)
+    base.fill(torch.from_numpy(kf).to(dev), torch.from_numpy(vf).to(dev))
+    del kf, vf
+    k_all = base.k.unsqueeze(0).repeat(n_rep, 1, 1, 1)
+    v_all = base.v.unsqueeze(0).repeat(n_rep, 1, 1, 1)
+    ctx0 = torch.full((n_rep,), C, dtype=torch.int32, device=dev)
+    ctx_all = ctx0.clone()
+    del base
+    caches = [CacheView(k_all[r], v_all[r], ctx_all[r:r + 1], hkv, D, cap) for r in range(n_rep)]
+
+    st = api.VerifyStep(N, hq, hkv, D, Wn, cap, V, max_depth=cfg.max_depth, device=dev)
+    launches_per_step = api.step_launches(N, hq, hkv, D, Wn, cap)
+
+    def one_step(i):
+        j = i % n_pool
+        st.run(caches[i % n_rep], q_all[j], tk_all[j], tv_all[j], par_all[j], tok_all[j],
+               lg_all[j])
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for i in range(4):                 # eager: sets kernel attributes before capture
+            one_step(i)
+        ctx_all.copy_(ctx0)
+    torch.cuda.synchronize()
+
+    def capture(nsteps, offset):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(nsteps):
+                one_step(offset + i)
+        ctx_all.copy_(ctx0)
+        torch.cuda.synchronize()
+        return g
+
+    g_warm = capture(Wu, 0)
+    g_timed = capture(K, Wu)
+
+    gpu_id = None
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        gpu_id = u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        gpu_id = None
+    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    clocks = ClockSampler(gpu_id, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv"))
+    clocks.start()
+
+    # ---- warm-up: W steps, repeated for about a second so clocks settle
+    t_end = time.time() + 1.5
+    with torch.cuda.stream(stream):
+        while True:
+            ctx_all.copy_(ctx0)
+            g_warm.replay()
+            stream.synchronize()
+            if time.time() >= t_end:
+                break
+        ctx_all.copy_(ctx0)
+    torch.cuda.synchronize()
+
+    # ---- timed: exactly K steps
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        g_timed.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    local_s = ev0.elapsed_time(ev1) / 1000.0
+    value, slowest = whole_job_value(local_s, K, world, device=dev)
+
+    # ---- per-entry-point durations (same kernels, events around each call,
+    # enqueued behind a spin kernel so the host never starves the GPU)
+    P = args.probe_steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(P)]
+    with torch.cuda.stream(stream):
+        ctx_all.copy_(ctx0)
+        torch.cuda._sleep(200_000_000)
+        for i in range(P):
+            j, c = i % n_pool, caches[i % n_rep]
+            e = evs[i]
+            e[0].record(stream)
+            api.tree_verify_attn(c, q_all[j], tk_all[j], tv_all[j], par_all[j], Wn, cfg.max_depth,
+                                 st.out, st.lse, st.ws[_accept_ws_bytes(api, N, V):])
+            e[1].record(stream)
+            api.greedy_accept(lg_all[j], par_all[j], tok_all[j], st.argmax, st.accept_len, st.path,
+                              st.out_tokens, st.ws)
+            e[2].record(stream)
+            api.kv_commit(c, st.accept_len, st.path, tk_all[j], tv_all[j])
+            e[3].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    t_attn = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) / 1000.0
+    t_acc = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) / 1000.0
+    t_com = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) / 1000.0
+
+    # ---- end to end through the API with pinned host inputs
+    e2e = run_e2e(args, api, cfg, steps_np, caches, ctx_all, ctx0, st, stream, dev)
+
+    status = int(st.status.item())
+    kv_b, lg_b, flops = algorithmic_per_step(cfg, [s.parent for s in steps_np])
+    ms = 1000.0 * slowest / K
+    per_rank_sps = K / slowest
+    kvlg_gbs = (kv_b + lg_b) * per_rank_sps / 1e9
+    peaks = _peaks()
+    hbm = peaks.get("hbm_gbs") or 6800.0
+    tf = peaks.get("bf16_tflops") or 1900.0
+    peak_src = "measured" if peaks else "fallback"
+
+    kernels = {
+        "dfv_tree_verify_attn": {"us": t_attn * 1e6, "tflops": flops / t_attn / 1e12,
+                                 "kv_gbs": kv_b / t_attn / 1e9},
+        "dfv_greedy_accept": {"us": t_acc * 1e6, "gbs": lg_b / t_acc / 1e9},
+        "dfv_kv_commit": {"us": t_com * 1e6},
+    }
+    dom = max(kernels, key=lambda k: kernels[k]["us"])
+    if dom == "dfv_tree_verify_attn":
+        roof = {"kernel": dom, "bound": "tensor", "achieved": flops / t_attn / 1e12, "peak": tf,
+                "unit": "TFLOP/s", "frac": flops / t_attn / 1e12 / tf, "traffic": None,
+                "peak_source": peak_src + " bf16 burst (f16 tensor rate taken equal)"}
+    else:
+        roof = {"kernel": dom, "bound": "hbm", "achieved": lg_b / t_acc / 1e9, "peak": hbm,
+                "unit": "GB/s", "frac": lg_b / t_acc / 1e9 / hbm, "traffic": None,
+                "peak_source": peak_src + " copy bandwidth"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        try:
+            r = run_cpu_oracle(args.cpu_seconds)
+            cpu = {"value": r["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
+                   "sample": r["sample"]}
+        except Exception as ex:  # reported, not fatal
+            cpu = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
+                   "sample": f"failed: {ex}"[:300]}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": Wu, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "ctx": C, "window": Wn, "budget": N - 1,
+                       "heads": f"{hq}/{hkv}", "head_dim": D, "vocab": V, "logits": "bf16",
+                       "kv": "Q4_0", "tree": "random depth<=16, planted path 8, p=0.8",
+                       "l2": f"inputs > L2: {n_pool} step inputs x 7.4 MB and {n_rep} "
+                             f"KV-cache replicas cycled", "graph": "one CUDA graph of K steps"},
+            "kv_logits_bytes_per_step": kv_b + lg_b,
+            "kv_logits_gbs": kvlg_gbs,
+            "kv_logits_frac_of_hbm": kvlg_gbs / hbm,
+            "roofline": roof,
+            "kernels": kernels,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * K,
+            "clocks": clk,
+            "device_status": status,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def _accept_ws_bytes(api, N, V):
+    n = api.accept_workspace_bytes(N, V)
+    return (n + 255) // 256 * 256
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+def run_e2e(args, api, cfg, steps_np, caches, ctx_all, ctx0, st, stream, dev):
+    """Same steps through the public API with inputs in pinned host memory:
+    each step copies its inputs host -> device, runs, and copies the
+    accepted tokens back (one CUDA graph of the copies and launches)."""
+    import numpy as np
+    import torch
+    n_steps = args.e2e_steps
+    N, hq, hkv, D, V = cfg.n_nodes, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.vocab
+
+    def pin(arrs, dtype):
+        t = torch.stack([torch.from_numpy(np.ascontiguousarray(a)) for a in arrs])
+        return t.view(dtype).pin_memory() if dtype is not None else t.pin_memory()
+
+    h_q = pin([s.q.view(np.int16) for s in steps_np], torch.bfloat16)
+    h_tk = pin([s.k_tree.view(np.int16) for s in steps_np], torch.bfloat16)
+    h_tv = pin([s.v_tree.view(np.int16) for s in steps_np], torch.bfloat16)
+    h_par = pin([s.parent for s in steps_np], None)
+    h_tok = pin([s.tokens for s in steps_np], None)
+    h_lg = pin([s.logits.view(np.int16) for s in steps_np], torch.bfloat16)
+    d_q = torch.empty_like(h_q[0], device=dev)
+    d_tk = torch.empty_like(h_tk[0], device=dev)
+    d_tv = torch.empty_like(h_tv[0], device=dev)
+    d_par = torch.empty_like(h_par[0], device=dev)
+    d_tok = torch.empty_like(h_tok[0], device=dev)
+    d_lg = torch.empty_like(h_lg[0], device=dev)
+    h_out_tok = torch.empty((n_steps, N), dtype=torch.int32).pin_memory()
+    h_acc = torch.empty((n_steps, 1), dtype=torch.int32).pin_memory()
+    h2d = sum(t[0].numel() * t.element_size() for t in (h_q, h_tk, h_tv, h_par, h_tok, h_lg))
+    d2h = h_out_tok[0].numel() * 4 + 4
+
+    def one(i):
+        j = i % len(steps_np)
+        for d, h in ((d_q, h_q), (d_tk, h_tk), (d_tv, h_tv), (d_par, h_par), (d_tok, h_tok),
+                     (d_lg, h_lg)):
+            d.copy_(h[j], non_blocking=True)
+        st.run(caches[i % len(caches)], d_q, d_tk, d_tv, d_par, d_tok, d_lg)
+        h_out_tok[i].copy_(st.out_tokens, non_blocking=True)
+        h_acc[i].copy_(st.accept_len, non_blocking=True)
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n_steps):
+            one(i)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            ctx_all.copy_(ctx0)
+            g.replay()
+        ctx_all.copy_(ctx0)
+        ev0.record(stream)
+        g.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    t = ev0.elapsed_time(ev1) / 1000.0
+    _, world, _ = dist_env()
+    value, _ = whole_job_value(t, n_steps, world, device=dev)
+    return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": n_steps, "note": "pinned host inputs copied in and accepted tokens copied "
+                                      "out every step, inside one CUDA graph"}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.cpu_child:
+        cpu_oracle_child(args.cpu_seconds, args.steps)
+        return
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

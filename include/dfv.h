@@ -234,6 +234,11 @@ dfv_status dfv_verify_step(int n_nodes, int max_depth, int n_q_heads, int n_kv_h
                            void* workspace, size_t workspace_bytes, uint32_t* status,
                            dfv_stream_t stream);
 
+/* Number of kernel launches one dfv_verify_step call makes for this shape
+ * (host-only query; -1 for an unsupported shape). */
+int dfv_verify_step_launches(int n_nodes, int n_q_heads, int n_kv_heads, int head_dim, int window,
+                             int cache_capacity);
+
 /* Zero `bytes` of a caller-owned workspace on `stream` (no allocation). */
 dfv_status dfv_workspace_clear(void* workspace, size_t bytes, dfv_stream_t stream);
 

@@ -24,6 +24,7 @@ SIGNATURES = {
     "dfv_kv_quantize_rows": (_i32, [_i32] * 6 + [_vp, _i32, _i64, _i64, _vp, _vp]),
     "dfv_verify_step_workspace_bytes": (_sz, [_i32] * 7),
     "dfv_verify_step": (_i32, [_i32] * 10 + [_vp] * 9 + [_f32] + [_vp] * 6 + [_vp, _sz, _vp, _vp]),
+    "dfv_verify_step_launches": (_i32, [_i32] * 6),
     "dfv_workspace_clear": (_i32, [_vp, _sz, _vp]),
 }
 

@@ -121,6 +121,11 @@ def step_workspace_bytes(n_nodes, n_q_heads, n_kv_heads, head_dim, window, capac
                                                  window, capacity, vocab)
 
 
+def step_launches(n_nodes, n_q_heads, n_kv_heads, head_dim, window, capacity):
+    return lib().dfv_verify_step_launches(n_nodes, n_q_heads, n_kv_heads, head_dim, window,
+                                          capacity)
+
+
 def workspace(nbytes, device="cuda", stream=None):
     """A zeroed, 256-byte aligned device workspace of ``nbytes``."""
     ws = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)

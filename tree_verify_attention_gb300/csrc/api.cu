@@ -25,6 +25,7 @@ dfv_status attn_launch(int n_nodes, int max_depth, int hq, int hkv, int head_dim
                        const void* tree_v, const int32_t* parent, float scale, float* out,
                        float* lse, void* workspace, size_t ws_bytes, uint32_t* status,
                        cudaStream_t stream);
+int attn_launches(int n_nodes, int hq, int hkv, int head_dim, int window, int cap);
 size_t accept_workspace_bytes(int n_nodes, int vocab);
 dfv_status accept_launch(int n_nodes, int vocab, int dtype, const void* logits,
                          const int32_t* parent, const int32_t* tokens, int32_t* argmax,
@@ -69,6 +70,13 @@ extern "C" size_t dfv_verify_step_workspace_bytes(int n_nodes, int n_q_heads, in
                                              cache_capacity);
   if (a == 0 || b == 0) return 0;
   return dfv::align256(a) + b;
+}
+
+extern "C" int dfv_verify_step_launches(int n_nodes, int n_q_heads, int n_kv_heads, int head_dim,
+                                        int window, int cache_capacity) {
+  const int a = dfv::attn_launches(n_nodes, n_q_heads, n_kv_heads, head_dim, window,
+                                   cache_capacity);
+  return a < 0 ? -1 : a + 2;   // attention (+ merge), argmax + walk, commit
 }
 
 extern "C" dfv_status dfv_verify_step(int n_nodes, int max_depth, int n_q_heads, int n_kv_heads,

@@ -528,6 +528,12 @@ size_t attn_workspace_bytes(int n_nodes, int hq, int hkv, int head_dim, int wind
   return attn_ws_bytes(attn_plan(n_nodes, hq, hkv, head_dim, window, cap), hkv, head_dim);
 }
 
+int attn_launches(int n_nodes, int hq, int hkv, int head_dim, int window, int cap) {
+  if (!attn_shape_ok(n_nodes, hq, hkv, head_dim, window, cap)) return -1;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return -1;
+  return attn_plan(n_nodes, hq, hkv, head_dim, window, cap).splits > 1 ? 2 : 1;
+}
+
 dfv_status attn_launch(int n_nodes, int max_depth, int hq, int hkv, int head_dim, int window,
                        int kv_format, int cap, const int32_t* ctx_len, const void* k_cache,
                        const void* v_cache, const void* q, const void* tree_k,
