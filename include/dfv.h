@@ -172,6 +172,38 @@ dfv_status dfv_greedy_accept(int n_nodes, int vocab, int logits_dtype, const voi
                              dfv_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * dfv_greedy_accept_static -- dfv_greedy_accept for callers that cannot
+ * allocate device memory. The paper has no counterpart; this is a library
+ * convenience.
+ *
+ * Same arguments, results and device status as dfv_greedy_accept, minus the
+ * workspace: the scratch lives in a device array of
+ * DFV_GREEDY_ACCEPT_STATIC_SCRATCH_BYTES bytes inside the library, which
+ * every GPU that loads the library holds until the process exits. Intended
+ * for code that is handed only its input and output buffers (for example a
+ * plugin whose host framework owns all device memory) or that must not call
+ * cudaMalloc / cudaFree because they can synchronise the device.
+ *
+ * - Returns DFV_ERR_WORKSPACE when the problem needs more scratch than the
+ *   array holds (dfv_greedy_accept_workspace_bytes(n_nodes, vocab) >
+ *   DFV_GREEDY_ACCEPT_STATIC_SCRATCH_BYTES); nothing is launched then.
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and caches it; make
+ *   that first call before any stream capture.
+ * - Each call clears the part of the array that must start at zero, in
+ *   stream order, before its kernel. All calls on a device share the array:
+ *   calls whose work overlaps on the GPU (different streams, no ordering)
+ *   race and give undefined results.
+ * - Allocates nothing: no cudaMalloc / cudaFree, no allocating library call.
+ * ---------------------------------------------------------------------- */
+#define DFV_GREEDY_ACCEPT_STATIC_SCRATCH_BYTES 16384
+
+dfv_status dfv_greedy_accept_static(int n_nodes, int vocab, int logits_dtype, const void* logits,
+                                    const int32_t* parent, const int32_t* tokens, int32_t* argmax,
+                                    int32_t* accept_len, int32_t* path, int32_t* out_tokens,
+                                    uint32_t* status, dfv_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * dfv_kv_commit -- commit the accepted rows, roll back the rest.
  *
  * Passage: "We got 207 tok/s with Qwen3.5-27B on an RTX 3090" (nowletus),

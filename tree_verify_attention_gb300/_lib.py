@@ -20,6 +20,7 @@ SIGNATURES = {
     "dfv_tree_verify_attn": (_i32, [_i32] * 8 + [_vp] * 7 + [_f32, _vp, _vp, _vp, _sz, _vp, _vp]),
     "dfv_greedy_accept_workspace_bytes": (_sz, [_i32, _i32]),
     "dfv_greedy_accept": (_i32, [_i32, _i32, _i32] + [_vp] * 7 + [_vp, _sz, _vp, _vp]),
+    "dfv_greedy_accept_static": (_i32, [_i32, _i32, _i32] + [_vp] * 7 + [_vp, _vp]),
     "dfv_kv_commit": (_i32, [_i32] * 5 + [_vp] * 7 + [_vp, _vp]),
     "dfv_kv_quantize_rows": (_i32, [_i32] * 6 + [_vp, _i32, _i64, _i64, _vp, _vp]),
     "dfv_verify_step_workspace_bytes": (_sz, [_i32] * 7),
