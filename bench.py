@@ -354,30 +354,21 @@ def run_gpu(args):
     local_s = ev0.elapsed_time(ev1) / 1000.0
     value, slowest = whole_job_value(local_s, K, world, device=dev)
 
-    # ---- per-entry-point durations (same kernels, events around each call,
-    # enqueued behind a spin kernel so the host never starves the GPU)
+    # ---- duration of the step kernel itself: events around each call,
+    # enqueued behind a spin kernel so the host never starves the GPU
     P = args.probe_steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(P)]
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(P)]
     with torch.cuda.stream(stream):
         ctx_all.copy_(ctx0)
         torch.cuda._sleep(200_000_000)
         for i in range(P):
-            j, c = i % n_pool, caches[i % n_rep]
-            e = evs[i]
-            e[0].record(stream)
-            api.tree_verify_attn(c, q_all[j], tk_all[j], tv_all[j], par_all[j], Wn, cfg.max_depth,
-                                 st.out, st.lse, st.ws[_accept_ws_bytes(api, N, V):])
-            e[1].record(stream)
-            api.greedy_accept(lg_all[j], par_all[j], tok_all[j], st.argmax, st.accept_len, st.path,
-                              st.out_tokens, st.ws)
-            e[2].record(stream)
-            api.kv_commit(c, st.accept_len, st.path, tk_all[j], tv_all[j])
-            e[3].record(stream)
+            evs[i][0].record(stream)
+            one_step(Wu + i)
+            evs[i][1].record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    t_attn = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) / 1000.0
-    t_acc = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) / 1000.0
-    t_com = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) / 1000.0
+    t_kernel = statistics.mean(a.elapsed_time(b) for a, b in evs) / 1000.0
 
     # ---- end to end through the API with pinned host inputs
     e2e = run_e2e(args, api, cfg, steps_np, caches, ctx_all, ctx0, st, stream, dev)
@@ -393,20 +384,17 @@ def run_gpu(args):
     peak_src = "measured" if peaks else "fallback"
 
     kernels = {
-        "dfv_tree_verify_attn": {"us": t_attn * 1e6, "tflops": flops / t_attn / 1e12,
-                                 "kv_gbs": kv_b / t_attn / 1e9},
-        "dfv_greedy_accept": {"us": t_acc * 1e6, "gbs": lg_b / t_acc / 1e9},
-        "dfv_kv_commit": {"us": t_com * 1e6},
+        "dfv_verify_step (step_kernel<256>)": {
+            "launches_per_step": launches_per_step, "us": t_kernel * 1e6,
+            "kv_logits_gbs": (kv_b + lg_b) / t_kernel / 1e9,
+            "attention_tflops": flops / t_kernel / 1e12},
     }
-    dom = max(kernels, key=lambda k: kernels[k]["us"])
-    if dom == "dfv_tree_verify_attn":
-        roof = {"kernel": dom, "bound": "tensor", "achieved": flops / t_attn / 1e12, "peak": tf,
-                "unit": "TFLOP/s", "frac": flops / t_attn / 1e12 / tf, "traffic": None,
-                "peak_source": peak_src + " bf16 burst (f16 tensor rate taken equal)"}
-    else:
-        roof = {"kernel": dom, "bound": "hbm", "achieved": lg_b / t_acc / 1e9, "peak": hbm,
-                "unit": "GB/s", "frac": lg_b / t_acc / 1e9 / hbm, "traffic": None,
-                "peak_source": peak_src + " copy bandwidth"}
+    roof = {"kernel": "step_kernel<256>", "bound": "hbm",
+            "achieved": (kv_b + lg_b) / t_kernel / 1e9, "peak": hbm, "unit": "GB/s",
+            "frac": (kv_b + lg_b) / t_kernel / 1e9 / hbm, "traffic": None,
+            "peak_source": peak_src + " copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+            "algorithmic_bytes": kv_b + lg_b,
+            "tensor_tflops": flops / t_kernel / 1e12, "tensor_peak": tf}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -443,11 +431,6 @@ def run_gpu(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
-
-
-def _accept_ws_bytes(api, N, V):
-    n = api.accept_workspace_bytes(N, V)
-    return (n + 255) // 256 * 256
 
 
 def _peaks():

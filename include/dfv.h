@@ -14,7 +14,7 @@
  *   dfv_greedy_accept     per-node vocabulary argmax + greedy tree walk
  *   dfv_kv_commit         Q4_0 re-quantisation of the accepted K/V rows into
  *                         the cache; rejected rows are never written
- *   dfv_verify_step       the three above, in order, on one stream
+ *   dfv_verify_step       the three above in one cooperative launch
  *
  * plus dfv_kv_quantize_rows, the same Q4_0 quantiser used to fill a cache
  * from float rows (prefill).
@@ -120,7 +120,9 @@ int dfv_version(void);
  *   out            device f32 [N][Hq][D]
  *   lse            device f32 [N][Hq] (natural-log log-sum-exp), may be NULL
  *   workspace      device scratch, >= dfv_tree_verify_attn_workspace_bytes()
- *                  bytes, 256-byte aligned; no initialisation needed
+ *                  bytes, 256-byte aligned; zero it once before its first use
+ *                  (dfv_workspace_clear); every call leaves it ready for the
+ *                  next
  *   status         device uint32[1] or NULL
  *
  * Value range: |q|, |tree_k|, |tree_v| and the cache values must stay within
@@ -247,11 +249,14 @@ dfv_status dfv_kv_quantize_rows(int n_kv_heads, int head_dim, int kv_format, int
                                 dfv_stream_t stream);
 
 /* ------------------------------------------------------------------------
- * dfv_verify_step -- one whole greedy tree-verify step: attention, argmax +
- * walk, commit, in that order on `stream`. Arguments as in the three entry
- * points above; `workspace` holds both scratch areas
- * (dfv_verify_step_workspace_bytes) and must be zeroed once before its
- * first use.
+ * dfv_verify_step -- one whole greedy tree-verify step (attention, argmax +
+ * walk, commit) in ONE cooperative kernel launch on `stream`: one CTA per SM,
+ * one grid-wide barrier between the streaming / tensor-core phase and the
+ * merge / walk / commit phase. Arguments and results as in the three entry
+ * points above; the committed length advances by the accept length.
+ * `workspace` (dfv_verify_step_workspace_bytes) must be zeroed once before
+ * its first use; each call leaves it ready for the next. Calls sharing a
+ * workspace must not overlap on the GPU.
  * ---------------------------------------------------------------------- */
 size_t dfv_verify_step_workspace_bytes(int n_nodes, int n_q_heads, int n_kv_heads, int head_dim,
                                        int window, int cache_capacity, int vocab);

@@ -94,8 +94,9 @@ __device__ __forceinline__ void block_argmax(float& best, int& bidx) {
 }
 
 // Argmax of one row chunk [begin, end), per thread; elements of each
-// thread are visited in increasing index order.
-template <typename T>
+// thread are visited in increasing index order. U vectors per thread are in
+// flight at once.
+template <typename T, int U = 4>
 __device__ __forceinline__ void chunk_argmax(const T* row, int begin, int end, float& best,
                                              int& bidx) {
   constexpr int VE = 16 / sizeof(T);
@@ -115,7 +116,6 @@ __device__ __forceinline__ void chunk_argmax(const T* row, int begin, int end, f
   const int vbeg = begin + head;
   const int nvec = (end - vbeg) / VE;
   const uint4* vp = reinterpret_cast<const uint4*>(row + vbeg);
-  constexpr int U = 4;
   for (int v0 = tid; v0 < nvec; v0 += U * kAcceptThreads) {
     uint4 r[U];
 #pragma unroll

@@ -18,26 +18,16 @@ int sm_count() {
   return cached[dev];
 }
 
-size_t attn_workspace_bytes(int n_nodes, int hq, int hkv, int head_dim, int window, int cap);
-dfv_status attn_launch(int n_nodes, int max_depth, int hq, int hkv, int head_dim, int window,
-                       int kv_format, int cap, const int32_t* ctx_len, const void* k_cache,
-                       const void* v_cache, const void* q, const void* tree_k,
-                       const void* tree_v, const int32_t* parent, float scale, float* out,
-                       float* lse, void* workspace, size_t ws_bytes, uint32_t* status,
-                       cudaStream_t stream);
-int attn_launches(int n_nodes, int hq, int hkv, int head_dim, int window, int cap);
-size_t accept_workspace_bytes(int n_nodes, int vocab);
-dfv_status accept_launch(int n_nodes, int vocab, int dtype, const void* logits,
-                         const int32_t* parent, const int32_t* tokens, int32_t* argmax,
-                         int32_t* accept_len, int32_t* path, int32_t* out_tokens,
-                         void* workspace, size_t ws_bytes, uint32_t* status,
-                         cudaStream_t stream);
-dfv_status commit_launch(int n_nodes, int n_kv_heads, int head_dim, int kv_format,
-                         int capacity, int32_t* ctx_len, const int32_t* accept_len,
-                         const int32_t* path, const void* tree_k, const void* tree_v,
-                         void* k_cache, void* v_cache, uint32_t* status, cudaStream_t stream);
-
-static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+size_t step_workspace_bytes(int n_nodes, int hq, int hkv, int head_dim, int window, int cap,
+                            int vocab, bool with_accept);
+dfv_status step_launch(bool with_accept, int n_nodes, int max_depth, int hq, int hkv,
+                       int head_dim, int window, int kv_format, int cap, int vocab,
+                       int logits_dtype, int32_t* ctx_len, void* k_cache, void* v_cache,
+                       const void* q, const void* tree_k, const void* tree_v,
+                       const int32_t* parent, const int32_t* tokens, const void* logits,
+                       float scale, float* out, float* lse, int32_t* argmax, int32_t* accept_len,
+                       int32_t* path, int32_t* out_tokens, void* workspace, size_t ws_bytes,
+                       uint32_t* status, cudaStream_t stream);
 
 }  // namespace dfv
 
@@ -62,21 +52,41 @@ extern "C" dfv_status dfv_workspace_clear(void* workspace, size_t bytes, dfv_str
              : DFV_ERR_CUDA;
 }
 
+extern "C" size_t dfv_tree_verify_attn_workspace_bytes(int n_nodes, int n_q_heads, int n_kv_heads,
+                                                       int head_dim, int window,
+                                                       int cache_capacity) {
+  return dfv::step_workspace_bytes(n_nodes, n_q_heads, n_kv_heads, head_dim, window,
+                                   cache_capacity, 0, false);
+}
+
+extern "C" dfv_status dfv_tree_verify_attn(int n_nodes, int max_depth, int n_q_heads,
+                                           int n_kv_heads, int head_dim, int window,
+                                           int kv_format, int cache_capacity,
+                                           const int32_t* ctx_len, const void* k_cache,
+                                           const void* v_cache, const void* q,
+                                           const void* tree_k, const void* tree_v,
+                                           const int32_t* parent, float scale, float* out,
+                                           float* lse, void* workspace, size_t workspace_bytes,
+                                           uint32_t* status, dfv_stream_t stream) {
+  return dfv::step_launch(false, n_nodes, max_depth, n_q_heads, n_kv_heads, head_dim, window,
+                          kv_format, cache_capacity, 0, 0, const_cast<int32_t*>(ctx_len),
+                          const_cast<void*>(k_cache), const_cast<void*>(v_cache), q, tree_k,
+                          tree_v, parent, nullptr, nullptr, scale, out, lse, nullptr, nullptr,
+                          nullptr, nullptr, workspace, workspace_bytes, status,
+                          static_cast<cudaStream_t>(stream));
+}
+
 extern "C" size_t dfv_verify_step_workspace_bytes(int n_nodes, int n_q_heads, int n_kv_heads,
                                                   int head_dim, int window, int cache_capacity,
                                                   int vocab) {
-  const size_t a = dfv::accept_workspace_bytes(n_nodes, vocab);
-  const size_t b = dfv::attn_workspace_bytes(n_nodes, n_q_heads, n_kv_heads, head_dim, window,
-                                             cache_capacity);
-  if (a == 0 || b == 0) return 0;
-  return dfv::align256(a) + b;
+  return dfv::step_workspace_bytes(n_nodes, n_q_heads, n_kv_heads, head_dim, window,
+                                   cache_capacity, vocab, true);
 }
 
 extern "C" int dfv_verify_step_launches(int n_nodes, int n_q_heads, int n_kv_heads, int head_dim,
                                         int window, int cache_capacity) {
-  const int a = dfv::attn_launches(n_nodes, n_q_heads, n_kv_heads, head_dim, window,
-                                   cache_capacity);
-  return a < 0 ? -1 : a + 2;   // attention (+ merge), argmax + walk, commit
+  return dfv::step_workspace_bytes(n_nodes, n_q_heads, n_kv_heads, head_dim, window,
+                                   cache_capacity, 1, true) ? 1 : -1;
 }
 
 extern "C" dfv_status dfv_verify_step(int n_nodes, int max_depth, int n_q_heads, int n_kv_heads,
@@ -90,26 +100,9 @@ extern "C" dfv_status dfv_verify_step(int n_nodes, int max_depth, int n_q_heads,
                                       int32_t* out_tokens, void* workspace,
                                       size_t workspace_bytes, uint32_t* status,
                                       dfv_stream_t stream) {
-  using namespace dfv;
-  if (n_nodes < 1 || n_nodes > kMaxNodes || vocab < 1) return DFV_ERR_INVALID;
-  const size_t need = dfv_verify_step_workspace_bytes(n_nodes, n_q_heads, n_kv_heads, head_dim,
-                                                      window, cache_capacity, vocab);
-  if (need == 0) return DFV_ERR_INVALID;
-  if (workspace == nullptr || !aligned(workspace, 256)) return DFV_ERR_INVALID;
-  if (workspace_bytes < need) return DFV_ERR_WORKSPACE;
-  // everything the later launches check, checked before the first launch
-  if (logits_dtype != DFV_DTYPE_F32 && logits_dtype != DFV_DTYPE_BF16) return DFV_ERR_UNSUPPORTED;
-  if (!logits || !tokens || !argmax || !accept_len || !path || !out_tokens) return DFV_ERR_INVALID;
-  const size_t a = align256(accept_workspace_bytes(n_nodes, vocab));
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  dfv_status st = attn_launch(n_nodes, max_depth, n_q_heads, n_kv_heads, head_dim, window,
-                              kv_format, cache_capacity, ctx_len, k_cache, v_cache, q, tree_k,
-                              tree_v, parent, scale, out, lse, static_cast<char*>(workspace) + a,
-                              workspace_bytes - a, status, s);
-  if (st != DFV_OK) return st;
-  st = accept_launch(n_nodes, vocab, logits_dtype, logits, parent, tokens, argmax, accept_len,
-                     path, out_tokens, workspace, a, status, s);
-  if (st != DFV_OK) return st;
-  return commit_launch(n_nodes, n_kv_heads, head_dim, kv_format, cache_capacity, ctx_len,
-                       accept_len, path, tree_k, tree_v, k_cache, v_cache, status, s);
+  return dfv::step_launch(true, n_nodes, max_depth, n_q_heads, n_kv_heads, head_dim, window,
+                          kv_format, cache_capacity, vocab, logits_dtype, ctx_len, k_cache,
+                          v_cache, q, tree_k, tree_v, parent, tokens, logits, scale, out, lse,
+                          argmax, accept_len, path, out_tokens, workspace, workspace_bytes,
+                          status, static_cast<cudaStream_t>(stream));
 }

@@ -1,0 +1,993 @@
+// The whole greedy tree-verify step in one cooperative launch, with the
+// attention on the 5th-generation tensor cores (tcgen05, TMEM accumulators).
+//
+// "Luce DFlash: Qwen3.6-27B ..." (ai-navigate-news, ja), feature list: DDTree
+// tree-verify (block 16, budget 22), greedy verification, Q4_0 KV cache,
+// sliding-window flash attention at decode (window 2048). The step computes,
+// for the N = budget + 1 tree nodes, attention over the visible committed
+// keys and the node's ancestors, the argmax of every node's logits, the
+// greedy walk, and the Q4_0 commit of the accepted rows.
+//
+// One CTA per SM, one launch per step, two phases around one grid barrier.
+//
+// Phase A, per CTA. At t = 0 thread 0 starts 1-D bulk copies (TMA engine)
+// of everything the CTA reads from HBM: its logits slice, the bf16 Q rows
+// of its attention tile and its Q4_0 K/V chunk (128 keys x 144 bytes each
+// at D = 256), so their latencies overlap. Then:
+//   * the logits slice is scanned from shared memory into a (max, lowest
+//     index) partial;
+//   * tree K/V rows are quantised to Q4_0 into a staging area (on CTAs
+//     without an attention unit when there are any), so the commit after
+//     the walk is a plain copy;
+//   * attention unit = (KV head h, 128-row tile of the head's (node, query
+//     head) rows, range of 128-key chunks). Q -> fp16, K and V dequantised
+//     ((q - 8) * d, one rounding), all in 128-byte-swizzled smem with keys or
+//     rows as the outer index; S = Q K^T by tcgen05.mma into TMEM (M = 128
+//     rows, N = 128 keys, K = D); two threads per row read S from TMEM, mask
+//     (window, ancestors), exchange the row max, exp2, write P (fp16);
+//     O += P V by tcgen05.mma (M = 128, N = D, K = 128 keys; V as an
+//     MN-major operand). The running max only moves (O rescaled in TMEM)
+//     when a chunk's max exceeds it by more than 2^8, so P <= 256 fits fp16.
+//     The row's normalised O (fp16), max and sum go to the workspace.
+// Grid barrier (bounded wait; a timeout sets DFV_DEV_TIMEOUT).
+// Phase B: CTAs 1..G-1 merge the key splits of a slice of the output rows
+// by log-sum-exp; CTA 0 merges the argmax partials, walks the tree in one
+// warp, copies the pre-quantised accepted rows into the cache at C..C+L-1
+// and advances the committed length (every CTA read it before the barrier).
+
+#include <math.h>
+
+#include "common.cuh"
+#include "accept_impl.cuh"
+#include "tc.cuh"
+
+namespace dfv {
+
+constexpr int kStepThreads = 256;
+constexpr int kRowsPerTile = 128;   // UMMA M
+constexpr int kChunk = 128;         // keys per chunk (UMMA N of S, K of P V)
+constexpr uint32_t kTmemCols = 512;
+constexpr int kMaxStepSplits = 256;
+constexpr float kRescaleLog2 = 8.0f;
+
+struct StepPlan {
+  int rows, n_mt, splits, units, grid, lunits, lchunks, lchunk_len, lbulk, smem;
+  size_t ws_bar, ws_arg, ws_qrows, ws_ml, ws_o, ws_total;
+};
+
+struct StepParams {
+  int n_nodes, max_depth, hq, hkv, group, window, capacity, vocab, logits_dtype;
+  int rows, n_mt, splits, units, lunits, lchunks, lchunk_len, lbulk;
+  int do_accept;
+  float scale_log2;
+  int32_t* ctx_len;
+  uint8_t* k_cache;
+  uint8_t* v_cache;
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* tree_k;
+  const __nv_bfloat16* tree_v;
+  const int32_t* parent;
+  const int32_t* tokens;
+  const void* logits;
+  float* out;
+  float* lse;
+  int32_t* argmax;
+  int32_t* accept_len;
+  int32_t* path;
+  int32_t* out_tokens;
+  unsigned int* bar;        // [0] arrivals, [1] generation
+  ArgPartial* arg_part;     // [lunits]
+  uint8_t* qrows;           // [N][Hkv][2][row bytes]
+  float2* part_ml;          // [units][128]  (running max, log2 units; sum)
+  __half* part_o;           // [units][128][D]  O / sum
+  uint32_t* status;
+};
+
+// Dynamic shared memory map (bytes from a 1024-aligned base).
+template <int D>
+struct StepSmem {
+  static constexpr int kRowB = D / 32 * 18;
+  static constexpr bool kBulk = (kRowB % 16) == 0;
+  static constexpr int kTileB = kRowsPerTile * D * 2;           // one [128][D] fp16 tile
+  static constexpr int kQ = 0;          // Q fp16 (swizzled); logits slice before that
+  static constexpr int kK = kQ + kTileB;  // K^ ; raw V lands here first; P later
+  static constexpr int kKBytes = kChunk * (D > kChunk ? D : kChunk) * 2;
+  static constexpr int kV = kK + kKBytes;  // V^ ; bf16 Q rows land here first
+  static constexpr int kRawK = kV + kTileB;
+  static constexpr int kBars = kRawK + (kBulk ? kChunk * kRowB : 0);
+  static constexpr int kBytes = kBars + 64 + 1024;   // + alignment slack
+};
+
+// ---------------------------------------------------------------- small helpers
+
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v);
+  uint4 o;
+  uint32_t* ov = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __bfloat1622float2(b[e]);
+    ov[e] = pack_half2(f.x, f.y);
+  }
+  return o;
+}
+
+// One Q4_0 block (2-byte aligned) -> 32 fp16 values in four 16-byte chunks:
+// chunk 0 = values 0..7, 1 = 8..15 (low nibbles), 2 = 16..23, 3 = 24..31.
+__device__ __forceinline__ void q4_0_block_chunks(const uint16_t* w, uint4* out) {
+  const __half dh = __ushort_as_half(w[0]);
+  const __half2 d2 = __halves2half2(dh, dh);
+  const __half2 bias = __float2half2_rn(1032.0f);
+  uint32_t* o = reinterpret_cast<uint32_t*>(out);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t u = w[1 + k];
+    const uint32_t lo = 0x64006400u | (u & 0x000Fu) | ((u & 0x0F00u) << 8);
+    const uint32_t hi = 0x64006400u | ((u >> 4) & 0x000Fu) | ((u & 0xF000u) << 4);
+    const __half2 vlo = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&lo), bias), d2);
+    const __half2 vhi = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&hi), bias), d2);
+    o[k] = *reinterpret_cast<const uint32_t*>(&vlo);        // chunks 0,1
+    o[8 + k] = *reinterpret_cast<const uint32_t*>(&vhi);    // chunks 2,3
+  }
+}
+
+// Bounded grid-wide barrier of a cooperative launch; false on timeout.
+__device__ bool grid_barrier(unsigned int* bar, unsigned int nblocks, uint32_t* status) {
+  __shared__ int s_gok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    volatile unsigned int* vgen = bar + 1;
+    const unsigned int gen = *vgen;
+    __threadfence();
+    const unsigned int arrived = atomicAdd(bar, 1u);
+    int ok = 1;
+    if (arrived == nblocks - 1) {
+      atomicExch(bar, 0u);
+      __threadfence();
+      atomicAdd(bar + 1, 1u);
+    } else {
+      uint32_t it = 0;
+      while (*vgen == gen) {
+        if (++it > (1u << 24)) { ok = 0; break; }
+        __nanosleep(32);
+      }
+    }
+    __threadfence();
+    if (!ok) report(status, DFV_DEV_TIMEOUT);
+    s_gok = ok;
+  }
+  __syncthreads();
+  return s_gok != 0;
+}
+
+// Thread 0 waits for an mbarrier phase; the CTA learns the outcome.
+__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int* s_flag,
+                                         uint32_t* status) {
+  if (threadIdx.x == 0) {
+    const bool ok = mbar_wait_bounded(bar, parity);
+    if (!ok) report(status, DFV_DEV_TIMEOUT);
+    *s_flag = ok ? 1 : 0;
+  }
+  __syncthreads();
+  return *s_flag != 0;
+}
+
+// ---------------------------------------------------------------- the kernel
+
+template <int D>
+__global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
+  using L = StepSmem<D>;
+  constexpr int NB = D / 32;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // swizzle atoms need 1024-byte aligned bases; the launch adds 1 KB of slack
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sQ = smem + L::kQ;
+  uint8_t* sK = smem + L::kK;
+  uint8_t* sV = smem + L::kV;
+  uint8_t* sRawK = smem + L::kRawK;
+  uint64_t* bar_kv = reinterpret_cast<uint64_t*>(smem + L::kBars);
+  uint64_t* bar_mma = bar_kv + 1;
+  uint64_t* bar_lg = bar_kv + 2;
+  uint64_t* bar_q = bar_kv + 3;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_kv + 4);
+
+  __shared__ int s_J[kMaxNodes], s_dep[kMaxNodes];
+  __shared__ uint32_t s_anc[kMaxNodes][kMaskWords];
+  __shared__ int s_row_node[kRowsPerTile], s_row_lo[kRowsPerTile];
+  __shared__ float s_pmax[2][kRowsPerTile];
+  __shared__ float s_m[kRowsPerTile], s_l[2][kRowsPerTile];
+  __shared__ int s_ok, s_C;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = gridDim.x, blk = blockIdx.x;
+  const int N = p.n_nodes;
+
+  int C = *p.ctx_len;
+  if (C < 0 || C > p.capacity) {
+    if (blk == 0 && tid == 0) report(p.status, DFV_DEV_CTX);
+    C = C < 0 ? 0 : p.capacity;
+  }
+  const int lo_min = p.window > 0 ? max(0, C - p.window + 1) : 0;
+  const int n_cc = (C - lo_min + kChunk - 1) / kChunk;        // committed chunks
+  const int T = n_cc + (N + kChunk - 1) / kChunk;              // + tree chunks
+
+  // ---- this CTA's attention unit
+  const int unit = blk < p.units ? blk : -1;
+  int h = 0, mt = 0, c0 = 0, c1 = 0;
+  if (unit >= 0) {
+    const int split = unit % p.splits;
+    mt = (unit / p.splits) % p.n_mt;
+    h = unit / (p.splits * p.n_mt);
+    c0 = static_cast<int>(static_cast<long>(split) * T / p.splits);
+    c1 = static_cast<int>(static_cast<long>(split + 1) * T / p.splits);
+  }
+  const int esz = p.logits_dtype == DFV_DTYPE_BF16 ? 2 : 4;
+
+  auto issue_kv = [&](int cc) {
+    // raw K -> sRawK, raw V -> sK (consumed before K is dequantised)
+    const int j0 = lo_min + cc * kChunk;
+    const int nk = min(kChunk, C - j0);
+    const uint32_t bytes = static_cast<uint32_t>(nk * L::kRowB);
+    const size_t off = (static_cast<size_t>(h) * p.capacity + j0) * L::kRowB;
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar_kv, 2 * bytes);
+    bulk_g2s(sRawK, p.k_cache + off, bytes, bar_kv);
+    bulk_g2s(sK, p.v_cache + off, bytes, bar_kv);
+  };
+  auto issue_logits = [&](int u) {
+    const int node = u / p.lchunks, ch = u % p.lchunks;
+    const int begin = ch * p.lchunk_len;
+    const int end = min(p.vocab, begin + p.lchunk_len);
+    const uint32_t bytes = end > begin ? static_cast<uint32_t>((end - begin) * esz) : 0u;
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar_lg, bytes);
+    if (bytes)
+      bulk_g2s(sQ, static_cast<const uint8_t*>(p.logits) +
+                       (static_cast<size_t>(node) * p.vocab + begin) * esz,
+               bytes, bar_lg);
+  };
+
+  // ================================================================ phase A
+  if (tid == 0) {
+    mbar_init(bar_kv, 1);
+    mbar_init(bar_mma, 1);
+    mbar_init(bar_lg, 1);
+    mbar_init(bar_q, 1);
+    fence_mbar_init();
+    if (p.do_accept && p.lbulk && blk < p.lunits) issue_logits(blk);
+    if (unit >= 0) {
+      // bf16 Q rows of the tile -> sV (row-major staging), one copy per
+      // node run of consecutive query heads
+      const int r0 = mt * kRowsPerTile;
+      const int r1 = min(p.rows, r0 + kRowsPerTile);
+      uint32_t total = 0;
+      for (int rg = r0; rg < r1;) {
+        const int j = rg % p.group;
+        const int run = min(p.group - j, r1 - rg);
+        total += static_cast<uint32_t>(run * D * 2);
+        rg += run;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar_q, total);
+      for (int rg = r0; rg < r1;) {
+        const int node = rg / p.group, j = rg % p.group;
+        const int run = min(p.group - j, r1 - rg);
+        bulk_g2s(sV + (rg - r0) * D * 2,
+                 p.q + (static_cast<size_t>(node) * p.hq + h * p.group + j) * D,
+                 static_cast<uint32_t>(run * D * 2), bar_q);
+        rg += run;
+      }
+      if constexpr (L::kBulk) {
+        if (c0 < c1 && c0 < n_cc) issue_kv(c0);
+      }
+    }
+  }
+  if (unit >= 0 && warp == 0) {
+    tc::tmem_alloc(s_tmem, kTmemCols);
+    tc::fence_before_sync();
+  }
+  int my_parent = -1;
+  if (unit >= 0 && tid < N) my_parent = tid == 0 ? -1 : p.parent[tid];
+  __syncthreads();   // barriers initialised
+
+  // ---- logits slice -> argmax partial
+  if (p.do_accept) {
+    uint32_t ph_lg = 0;
+    for (int u = blk; u < p.lunits; u += G) {
+      const int node = u / p.lchunks, ch = u % p.lchunks;
+      const int begin = ch * p.lchunk_len;
+      const int end = min(p.vocab, begin + p.lchunk_len);
+      float best = -INFINITY;
+      int bidx = INT_MAX;
+      if (p.lbulk) {
+        if (u != blk && tid == 0) issue_logits(u);
+        if (!cta_wait(bar_lg, ph_lg, &s_ok, p.status)) break;
+        ph_lg ^= 1u;
+        const int nvec = end > begin ? (end - begin) * esz / 16 : 0;
+        const uint4* sv = reinterpret_cast<const uint4*>(sQ);
+        if (esz == 2) {
+          for (int v = tid; v < nvec; v += kStepThreads)
+            scan_vec<__nv_bfloat16>(sv[v], begin + v * 8, best, bidx);
+        } else {
+          for (int v = tid; v < nvec; v += kStepThreads)
+            scan_vec<float>(sv[v], begin + v * 4, best, bidx);
+        }
+      } else if (esz == 2) {
+        chunk_argmax<__nv_bfloat16, 16>(
+            static_cast<const __nv_bfloat16*>(p.logits) + static_cast<size_t>(node) * p.vocab,
+            begin, end, best, bidx);
+      } else {
+        chunk_argmax<float, 16>(static_cast<const float*>(p.logits) + static_cast<size_t>(node) * p.vocab,
+                                begin, end, best, bidx);
+      }
+      block_argmax(best, bidx);
+      if (tid == 0) {
+        p.arg_part[u].v = best;
+        p.arg_part[u].idx = bidx;
+      }
+      __syncthreads();   // the slice buffer is reused
+    }
+    // ---- pre-quantise tree rows, on the CTAs without an attention unit
+    // when there are any, else spread over all CTAs
+    const int tot = N * p.hkv * 2 * NB;
+    const int q0 = G > p.units ? p.units : 0;
+    const int nq = G - q0;
+    if (blk >= q0) {
+      const int b0 = static_cast<int>(static_cast<long>(blk - q0) * tot / nq);
+      const int b1 = static_cast<int>(static_cast<long>(blk - q0 + 1) * tot / nq);
+      for (int it = b0 + tid; it < b1; it += kStepThreads) {
+        const int b = it % NB;
+        const int kv = (it / NB) & 1;
+        const int hh = (it / (2 * NB)) % p.hkv;
+        const int t = it / (2 * NB * p.hkv);
+        const uint4* v = reinterpret_cast<const uint4*>(
+            (kv ? p.tree_v : p.tree_k) + (static_cast<size_t>(t) * p.hkv + hh) * D + b * 32);
+        uint4 r4[4];
+#pragma unroll
+        for (int u4 = 0; u4 < 4; ++u4) r4[u4] = v[u4];
+        float x[32];
+#pragma unroll
+        for (int u4 = 0; u4 < 4; ++u4) {
+          const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&r4[u4]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(hb[e]);
+            x[u4 * 8 + 2 * e] = f.x;
+            x[u4 * 8 + 2 * e + 1] = f.y;
+          }
+        }
+        q4_0_quantize_block(x, p.qrows + ((static_cast<size_t>(t) * p.hkv + hh) * 2 + kv) * L::kRowB +
+                                   b * 18);
+      }
+    }
+  }
+
+  if (unit >= 0) {
+    // ---- tree: depth and ancestor-or-self masks by pointer jumping;
+    // ceil(log2 N) rounds cover every depth (< N)
+    if (tid < N) {
+      int pa = my_parent;
+      if (tid > 0 && (pa < 0 || pa >= tid)) {
+        if (blk == 0) report(p.status, DFV_DEV_BAD_TREE);
+        pa = 0;
+      }
+      s_J[tid] = pa;
+      s_dep[tid] = tid > 0 ? 1 : 0;
+#pragma unroll
+      for (int w = 0; w < kMaskWords; ++w)
+        s_anc[tid][w] = (tid >> 5) == w ? (1u << (tid & 31)) : 0u;
+    }
+    int rounds = 0;
+    while ((1 << rounds) < N) ++rounds;
+    __syncthreads();
+#pragma unroll 1
+    for (int round = 0; round < rounds; ++round) {
+      int j = -1, nd = 0, nj = -1;
+      uint32_t nm[kMaskWords];
+      if (tid < N) {
+        j = s_J[tid];
+        if (j >= 0) {
+          nd = s_dep[tid] + s_dep[j];
+          nj = s_J[j];
+#pragma unroll
+          for (int w = 0; w < kMaskWords; ++w) nm[w] = s_anc[tid][w] | s_anc[j][w];
+        }
+      }
+      __syncthreads();
+      if (tid < N && j >= 0) {
+        s_dep[tid] = nd;
+        s_J[tid] = nj;
+#pragma unroll
+        for (int w = 0; w < kMaskWords; ++w) s_anc[tid][w] = nm[w];
+      }
+      __syncthreads();
+    }
+    if (blk == 0 && tid < N && s_dep[tid] > p.max_depth) report(p.status, DFV_DEV_DEPTH);
+    if (tid < kRowsPerTile) {
+      const int rg = mt * kRowsPerTile + tid;
+      if (rg < p.rows) {
+        const int node = rg / p.group;
+        s_row_node[tid] = node;
+        s_row_lo[tid] = p.window > 0 ? C + s_dep[node] - p.window + 1 : 0;
+      } else {
+        s_row_node[tid] = -1;
+        s_row_lo[tid] = 0x7fffffff;
+      }
+    }
+    // ---- Q: staged bf16 rows (sV) -> fp16 swizzled (sQ)
+    const bool q_ok = cta_wait(bar_q, 0, &s_ok, p.status);
+    if (q_ok) {
+      constexpr int QU = kRowsPerTile * (D / 8) / kStepThreads;
+#pragma unroll
+      for (int u = 0; u < QU; ++u) {
+        const int it = tid + u * kStepThreads;
+        const int lr = it / (D / 8), c = it % (D / 8);
+        const uint4 v = mt * kRowsPerTile + lr < p.rows
+                            ? *reinterpret_cast<const uint4*>(sV + lr * D * 2 + c * 16)
+                            : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(sQ + tc::sw128_offset(lr, c, kRowsPerTile)) = bf16x8_to_f16x8(v);
+      }
+    }
+    __syncthreads();
+    tc::fence_after_sync();
+
+    const uint32_t tmem = *s_tmem;
+    const uint32_t t_s = tmem;              // S: columns [0, 128)
+    const uint32_t t_o = tmem + kChunk;     // O: columns [128, 128 + D)
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int r = (warp & 3) * 32 + lane;   // this thread's row
+    const int hc = warp >> 2;               // its half of the keys / of O's columns
+    uint32_t ph_kv = 0, ph_mma = 0;
+    float m_run = -INFINITY, l_half = 0.f;
+    bool o_valid = false, alive = q_ok;
+
+#pragma unroll 1
+    for (int cc = c0; cc < c1 && alive; ++cc) {
+      const bool committed = cc < n_cc;
+      const int j0 = lo_min + cc * kChunk;
+      const int nk = committed ? min(kChunk, C - j0) : 0;
+      if (committed) {
+        if constexpr (L::kBulk) {
+          if (tid == 0 && cc != c0) issue_kv(cc);
+          if (!cta_wait(bar_kv, ph_kv, &s_ok, p.status)) { alive = false; break; }
+          ph_kv ^= 1u;
+        }
+        // V: raw (sK or global) -> sV [keys][D]; then K: raw -> sK [keys][D]
+#pragma unroll 1
+        for (int kvi = 1; kvi >= 0; --kvi) {
+          uint8_t* dst = kvi ? sV : sK;
+          const uint8_t* base;
+          if constexpr (L::kBulk) base = kvi ? sK : sRawK;
+          else base = (kvi ? p.v_cache : p.k_cache) + (static_cast<size_t>(h) * p.capacity + j0) * L::kRowB;
+          for (int it = tid; it < kChunk * NB; it += kStepThreads) {
+            const int key = it / NB, b = it % NB;
+            uint4 o4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o4[e] = make_uint4(0, 0, 0, 0);
+            if (key < nk)
+              q4_0_block_chunks(reinterpret_cast<const uint16_t*>(base + key * L::kRowB + b * 18), o4);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              *reinterpret_cast<uint4*>(dst + tc::sw128_offset(key, b * 4 + e, kChunk)) = o4[e];
+          }
+          __syncthreads();   // raw V (in sK) consumed before K overwrites it
+        }
+      } else {
+        // tree chunk: keys t = 0..N-1 from tree_k / tree_v (bf16 -> fp16)
+        const int t0 = (cc - n_cc) * kChunk;
+        for (int it = tid; it < 2 * kChunk * (D / 8); it += kStepThreads) {
+          const int kvi = it / (kChunk * (D / 8));
+          const int key = (it / (D / 8)) % kChunk, c = it % (D / 8);
+          const int t = t0 + key;
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (t < N)
+            v = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(
+                (kvi ? p.tree_v : p.tree_k) + (static_cast<size_t>(t) * p.hkv + h) * D + c * 8));
+          *reinterpret_cast<uint4*>((kvi ? sV : sK) + tc::sw128_offset(key, c, kChunk)) = v;
+        }
+      }
+      fence_proxy_async_smem();
+      __syncthreads();
+
+      // ---- S = Q K^T (M = 128 rows, N = 128 keys, K = D)
+      if (tid == 0) {
+        tc::fence_after_sync();
+        const uint32_t idesc = tc::idesc_f16(kRowsPerTile, kChunk);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = static_cast<uint32_t>((kk >> 2) * kRowsPerTile * 128 + (kk & 3) * 32);
+          tc::mma_f16(t_s, tc::smem_desc_sw128(smem_u32(sQ) + off, 1024),
+                      tc::smem_desc_sw128(smem_u32(sK) + off, 1024), idesc, kk > 0 ? 1u : 0u);
+        }
+        tc::commit(bar_mma);
+      }
+      if (!cta_wait(bar_mma, ph_mma, &s_ok, p.status)) { alive = false; break; }
+      ph_mma ^= 1u;
+      tc::fence_after_sync();
+
+      // ---- masked softmax: two threads per row, 64 keys each
+      {
+        const int kb0 = hc * 64;
+        float s[64];
+        tc::ld32(t_s + lane_base + kb0, s);
+        tc::ld32(t_s + lane_base + kb0 + 32, s + 32);
+        const int node = s_row_node[r], lo = s_row_lo[r];
+        float cm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        const float sc = p.scale_log2;
+        if (committed) {
+          // visible keys of this row form the range [kmin, kmax)
+          const int kmin = min(max(lo - j0, 0), kChunk) - kb0;
+          const int kmax = (node >= 0 ? nk : 0) - kb0;
+#pragma unroll
+          for (int k = 0; k < 64; ++k) {
+            const float x = (k >= kmin && k < kmax) ? s[k] * sc : -INFINITY;
+            s[k] = x;
+            cm[k & 3] = fmaxf(cm[k & 3], x);
+          }
+        } else {
+          // tree keys t = 0..N-1 (N <= 65 < 128: one tree chunk)
+          uint32_t mw0 = 0u, mw1 = 0u;
+          if (node >= 0) {
+            mw0 = s_anc[node][hc * 2];
+            mw1 = hc == 0 ? s_anc[node][1] : 0u;
+          }
+#pragma unroll
+          for (int k = 0; k < 64; ++k) {
+            const uint32_t w = k < 32 ? mw0 : mw1;
+            const float x = ((w >> (k & 31)) & 1u) ? s[k] * sc : -INFINITY;
+            s[k] = x;
+            cm[k & 3] = fmaxf(cm[k & 3], x);
+          }
+        }
+        s_pmax[hc][r] = fmaxf(fmaxf(cm[0], cm[1]), fmaxf(cm[2], cm[3]));
+        __syncthreads();
+        const float cmax = fmaxf(s_pmax[0][r], s_pmax[1][r]);
+        float alpha = 1.f;
+        bool rescale = false;
+        if (m_run == -INFINITY) {
+          m_run = cmax;                       // O and l are still zero
+        } else if (cmax > m_run + kRescaleLog2) {
+          alpha = tc::ex2(m_run - cmax);
+          rescale = true;
+          m_run = cmax;
+        }
+        const float sub = m_run == -INFINITY ? 0.f : m_run;
+        float rs = 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float p0 = tc::ex2(s[c * 8 + 2 * e] - sub);
+            const float p1 = tc::ex2(s[c * 8 + 2 * e + 1] - sub);
+            rs += p0 + p1;
+            w4[e] = pack_half2(p0, p1);
+          }
+          *reinterpret_cast<uint4*>(sK + tc::sw128_offset(r, hc * 8 + c, kRowsPerTile)) =
+              make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+        l_half = l_half * alpha + rs;
+        if (o_valid && __any_sync(0xffffffffu, rescale)) {
+          // this warp's half of the row's O columns
+          for (int c = 0; c < D / 64; ++c) {
+            const uint32_t col = static_cast<uint32_t>(hc * (D / 2) + c * 32);
+            float ov[32];
+            tc::ld32(t_o + lane_base + col, ov);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] *= alpha;
+            tc::st32(t_o + lane_base + col, ov);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      tc::fence_before_sync();
+      __syncthreads();
+
+      // ---- O += P V (M = 128 rows, N = D, K = 128 keys; V MN-major)
+      if (tid == 0) {
+        tc::fence_after_sync();
+        const uint32_t idesc = tc::idesc_f16(kRowsPerTile, D, true);
+#pragma unroll
+        for (int kk = 0; kk < kChunk / 16; ++kk) {
+          const uint32_t offa = static_cast<uint32_t>((kk >> 2) * kRowsPerTile * 128 + (kk & 3) * 32);
+          const uint32_t offb = static_cast<uint32_t>(kk * 16 * 128);
+          tc::mma_f16(t_o, tc::smem_desc_sw128(smem_u32(sK) + offa, 1024),
+                      tc::smem_desc_sw128_mn(smem_u32(sV) + offb, kChunk * 128, 1024), idesc,
+                      (o_valid || kk > 0) ? 1u : 0u);
+        }
+        tc::commit(bar_mma);
+      }
+      if (!cta_wait(bar_mma, ph_mma, &s_ok, p.status)) { alive = false; break; }
+      ph_mma ^= 1u;
+      o_valid = true;
+      tc::fence_after_sync();
+    }
+
+    // ---- epilogue: O rows from TMEM -> workspace (or the output when
+    // there is one split); 32 x 32 blocks go through smem (sQ is free) so
+    // that global stores are row-contiguous
+    s_l[hc][r] = l_half;
+    if (hc == 0) s_m[r] = m_run;
+    __syncthreads();
+    {
+      float* stage = reinterpret_cast<float*>(sQ) + warp * (32 * 36);
+      for (int c = 0; c < D / 64; ++c) {
+        const int col = hc * (D / 2) + c * 32;
+        float ov[32];
+        tc::ld32(t_o + lane_base + col, ov);
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(stage + lane * 36 + e) = make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = i * 4 + (lane >> 3);             // row within the warp's 32
+          const int row = (warp & 3) * 32 + rr;
+          const int rg = mt * kRowsPerTile + row;
+          float4 v = *reinterpret_cast<const float4*>(stage + rr * 36 + (lane & 7) * 4);
+          const float l = s_l[0][row] + s_l[1][row];
+          if (rg < p.rows && o_valid && alive && l > 0.f) {
+            const float inv = 1.f / l;
+            v.x *= inv; v.y *= inv; v.z *= inv; v.w *= inv;
+            if (p.splits == 1) {
+              const int node = rg / p.group, qh = h * p.group + rg % p.group;
+              *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(node) * p.hq + qh) * D + col +
+                                         (lane & 7) * 4) = v;
+            } else {
+              __half2 h01 = __floats2half2_rn(v.x, v.y), h23 = __floats2half2_rn(v.z, v.w);
+              uint2 hv;
+              hv.x = *reinterpret_cast<uint32_t*>(&h01);
+              hv.y = *reinterpret_cast<uint32_t*>(&h23);
+              *reinterpret_cast<uint2*>(p.part_o + (static_cast<size_t>(unit) * kRowsPerTile + row) * D +
+                                        col + (lane & 7) * 4) = hv;
+            }
+          }
+        }
+        __syncwarp();
+      }
+      const int rg = mt * kRowsPerTile + r;
+      if (hc == 0 && rg < p.rows) {
+        const float m = s_m[r], l = s_l[0][r] + s_l[1][r];
+        const bool ok = o_valid && alive && l > 0.f;
+        if (p.splits == 1) {
+          const int node = rg / p.group, qh = h * p.group + rg % p.group;
+          if (p.lse != nullptr) p.lse[node * p.hq + qh] = (m + log2f(l)) * 0.69314718055994531f;
+        } else {
+          p.part_ml[static_cast<size_t>(unit) * kRowsPerTile + r] =
+              make_float2(ok ? m : -INFINITY, ok ? l : 0.f);
+        }
+      }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+  }
+  if (tid == 0) s_C = C;
+
+  // ================================================================ barrier
+  if (!grid_barrier(p.bar, static_cast<unsigned int>(G), p.status)) return;
+
+  // ---- merge the key splits of a slice of the output rows (CTA 0 is kept
+  // free for the walk when the step has one)
+  if (p.splits > 1) {
+    const int c0b = (p.do_accept && G > 1) ? 1 : 0;
+    const int nb = G - c0b;
+    const int total = p.hkv * p.rows;
+    if (blk >= c0b) {
+      const int r0 = static_cast<int>(static_cast<long>(blk - c0b) * total / nb);
+      const int r1 = static_cast<int>(static_cast<long>(blk - c0b + 1) * total / nb);
+      for (int it = tid; it < (r1 - r0) * (D / 4); it += kStepThreads) {
+        const int gr = r0 + it / (D / 4), d = (it % (D / 4)) * 4;
+        const int hh = gr / p.rows, rg = gr % p.rows;
+        const int mtt = rg / kRowsPerTile, rr = rg % kRowsPerTile;
+        const size_t ubase = static_cast<size_t>(hh * p.n_mt + mtt) * p.splits;
+        constexpr int SB = 24;
+        float M = -INFINITY, lsum = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s0 = 0; s0 < p.splits; s0 += SB) {
+          float2 ml[SB];
+          uint2 ov[SB];
+#pragma unroll
+          for (int u = 0; u < SB; ++u) {
+            ml[u] = make_float2(-INFINITY, 0.f);
+            ov[u] = make_uint2(0u, 0u);
+            if (s0 + u < p.splits) {
+              const size_t row = (ubase + s0 + u) * kRowsPerTile + rr;
+              ml[u] = __ldcg(&p.part_ml[row]);
+              ov[u] = __ldcg(reinterpret_cast<const uint2*>(p.part_o + row * D + d));
+            }
+          }
+          float Mb = M;
+#pragma unroll
+          for (int u = 0; u < SB; ++u) Mb = fmaxf(Mb, ml[u].x);
+          if (Mb == -INFINITY) continue;
+          const float a = M == -INFINITY ? 0.f : tc::ex2(M - Mb);
+          lsum *= a;
+          acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
+          M = Mb;
+#pragma unroll
+          for (int u = 0; u < SB; ++u) {
+            if (ml[u].x == -INFINITY) continue;
+            const float w = tc::ex2(ml[u].x - M) * ml[u].y;
+            const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&ov[u].x));
+            const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&ov[u].y));
+            lsum += w;
+            acc.x += w * f01.x;
+            acc.y += w * f01.y;
+            acc.z += w * f23.x;
+            acc.w += w * f23.y;
+          }
+        }
+        const float inv = 1.f / lsum;
+        const int node = rg / p.group, qh = hh * p.group + rg % p.group;
+        *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(node) * p.hq + qh) * D + d) =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        if (d == 0 && p.lse != nullptr)
+          p.lse[node * p.hq + qh] = (M + log2f(lsum)) * 0.69314718055994531f;
+      }
+    }
+  }
+
+  // ---- CTA 0: argmax merge, walk, commit
+  if (p.do_accept && blk == 0) {
+    __shared__ int s_am[kMaxNodes];
+    __shared__ int s_path[kMaxNodes];
+    __shared__ int s_L;
+    for (int node = warp; node < N; node += kStepThreads / 32) {
+      float best = -INFINITY;
+      int bidx = INT_MAX;
+      for (int c = lane; c < p.lchunks; c += 32) {
+        const ArgPartial* ap = p.arg_part + node * p.lchunks + c;
+        const float v = __ldcg(&ap->v);
+        const int i = __ldcg(&ap->idx);
+        if (beats(v, i, best, bidx)) { best = v; bidx = i; }
+      }
+      warp_argmax(best, bidx);
+      if (lane == 0) {
+        s_am[node] = bidx;
+        p.argmax[node] = bidx;
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int par[3], tok[3];
+#pragma unroll
+      for (int s = 0; s < 3; ++s) {
+        const int n = lane + 32 * s;
+        par[s] = -2;
+        tok[s] = 0;
+        if (n >= 1 && n < N) {
+          int pa = p.parent[n];
+          if (pa < 0 || pa >= n) pa = 0;
+          par[s] = pa;
+          tok[s] = p.tokens[n];
+        }
+      }
+      int cur = 0, Lw = 1;
+      if (lane == 0) s_path[0] = 0;
+      for (int itw = 0; itw < N; ++itw) {
+        const int t = s_am[cur];
+        const unsigned b0 = __ballot_sync(0xffffffffu, par[0] == cur && tok[0] == t);
+        const unsigned b1 = __ballot_sync(0xffffffffu, par[1] == cur && tok[1] == t);
+        const unsigned b2 = __ballot_sync(0xffffffffu, par[2] == cur && tok[2] == t);
+        int next = -1;
+        if (b0) next = __ffs(b0) - 1;
+        else if (b1) next = 31 + __ffs(b1);
+        else if (b2) next = 63 + __ffs(b2);
+        if (next < 0) break;
+        if (lane == 0) s_path[Lw] = next;
+        ++Lw;
+        cur = next;
+      }
+      __syncwarp();
+      for (int k = lane; k < N; k += 32) {
+        p.path[k] = k < Lw ? s_path[k] : -1;
+        int ot = -1;
+        if (k < Lw - 1) ot = p.tokens[s_path[k + 1]];
+        else if (k == Lw - 1) ot = s_am[s_path[Lw - 1]];
+        p.out_tokens[k] = ot;
+      }
+      if (lane == 0) {
+        *p.accept_len = Lw;
+        s_L = Lw;
+      }
+    }
+    __syncthreads();
+    const int Lc = s_L, Cc = s_C;
+    if (Cc + Lc > p.capacity) {
+      if (tid == 0) report(p.status, DFV_DEV_CAPACITY);
+    } else {
+      constexpr int W4 = L::kRowB / 4;
+      const int total = Lc * p.hkv * 2 * W4;
+      for (int it = tid; it < total; it += kStepThreads) {
+        const int w = it % W4;
+        const int kv = (it / W4) & 1;
+        const int hh = (it / (2 * W4)) % p.hkv;
+        const int k = it / (2 * W4 * p.hkv);
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(
+            p.qrows + ((static_cast<size_t>(s_path[k]) * p.hkv + hh) * 2 + kv) * L::kRowB);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(
+            (kv ? p.v_cache : p.k_cache) + (static_cast<size_t>(hh) * p.capacity + Cc + k) * L::kRowB);
+        dst[w] = __ldcg(src + w);
+      }
+      __syncthreads();
+      if (tid == 0) *p.ctx_len = Cc + Lc;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+static size_t a256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, int cap, int vocab,
+                      int logits_dtype, bool with_accept, StepPlan* pl) {
+  if (n_nodes < 1 || n_nodes > kMaxNodes || hkv < 1 || hq < hkv || hq % hkv || hq > 256 ||
+      window < 0 || cap < 0)
+    return false;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return false;
+  if (with_accept && vocab < 1) return false;
+  const int sms = sm_count();
+  pl->grid = sms;
+  pl->rows = n_nodes * (hq / hkv);
+  pl->n_mt = (pl->rows + kRowsPerTile - 1) / kRowsPerTile;
+  const long kbound = window > 0 ? (window - 1 < cap ? window - 1 : cap) : cap;
+  const long tb = (kbound + kChunk - 1) / kChunk + (n_nodes + kChunk - 1) / kChunk;
+  long s = sms / (hkv * pl->n_mt);
+  if (s > tb) s = tb;
+  if (s > kMaxStepSplits) s = kMaxStepSplits;
+  if (s < 1) return false;                      // more (head, tile) pairs than SMs
+  pl->splits = static_cast<int>(s);
+  pl->units = hkv * pl->n_mt * pl->splits;
+  const int tile_b = kRowsPerTile * head_dim * 2;        // logits staging bytes
+  const int esz = logits_dtype == DFV_DTYPE_BF16 ? 2 : 4;
+  if (with_accept) {
+    // slices: one per CTA when they fit the staging area, more otherwise;
+    // bulk-copied when every slice starts and ends 16-byte aligned
+    int lc = sms / n_nodes;
+    if (lc < 1) lc = 1;
+    const int per = tile_b / esz;
+    const int need = (vocab + per - 1) / per;
+    if (lc < need) lc = need;
+    const int cap_c = (vocab + 255) / 256;
+    if (lc > cap_c) lc = cap_c < need ? need : cap_c;
+    pl->lchunks = lc;
+    pl->lunits = n_nodes * lc;
+    const int align_el = 16 / esz;
+    pl->lchunk_len = (((vocab + lc - 1) / lc) + align_el - 1) / align_el * align_el;
+    pl->lbulk = (static_cast<long>(vocab) * esz % 16 == 0) && pl->lchunk_len * esz <= tile_b;
+  } else {
+    pl->lchunks = pl->lunits = pl->lchunk_len = pl->lbulk = 0;
+  }
+  switch (head_dim) {
+    case 64: pl->smem = StepSmem<64>::kBytes; break;
+    case 128: pl->smem = StepSmem<128>::kBytes; break;
+    default: pl->smem = StepSmem<256>::kBytes; break;
+  }
+  const int rowb = head_dim / 32 * 18;
+  pl->ws_bar = 0;
+  pl->ws_arg = 256;
+  pl->ws_qrows = pl->ws_arg + a256(static_cast<size_t>(pl->lunits) * sizeof(ArgPartial));
+  pl->ws_ml = pl->ws_qrows + a256(with_accept ? static_cast<size_t>(n_nodes) * hkv * 2 * rowb : 0);
+  const size_t nrow = pl->splits > 1 ? static_cast<size_t>(pl->units) * kRowsPerTile : 0;
+  pl->ws_o = pl->ws_ml + a256(nrow * sizeof(float2));
+  pl->ws_total = pl->ws_o + a256(nrow * head_dim * sizeof(__half));
+  return true;
+}
+
+template <int D>
+static dfv_status step_launch_d(StepParams& p, const StepPlan& pl, cudaStream_t stream) {
+  static int configured[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DFV_ERR_CUDA;
+  if (!configured[dev]) {
+    if (cudaFuncSetAttribute(step_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             StepSmem<D>::kBytes) != cudaSuccess)
+      return DFV_ERR_CUDA;
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, step_kernel<D>, kStepThreads,
+                                                      StepSmem<D>::kBytes) != cudaSuccess ||
+        nb < 1)
+      return DFV_ERR_CUDA;
+    configured[dev] = 1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.grid);
+  cfg.blockDim = dim3(kStepThreads);
+  cfg.dynamicSmemBytes = StepSmem<D>::kBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, step_kernel<D>, p) == cudaSuccess ? DFV_OK : DFV_ERR_CUDA;
+}
+
+// Workspace of either logits element size (the slicing differs slightly).
+size_t step_workspace_bytes(int n_nodes, int hq, int hkv, int head_dim, int window, int cap,
+                            int vocab, bool with_accept) {
+  StepPlan a, b;
+  if (!step_plan(n_nodes, hq, hkv, head_dim, window, cap, vocab, DFV_DTYPE_F32, with_accept, &a))
+    return 0;
+  step_plan(n_nodes, hq, hkv, head_dim, window, cap, vocab, DFV_DTYPE_BF16, with_accept, &b);
+  return a.ws_total > b.ws_total ? a.ws_total : b.ws_total;
+}
+
+// Attention only (with_accept = false) or the whole step.
+dfv_status step_launch(bool with_accept, int n_nodes, int max_depth, int hq, int hkv,
+                       int head_dim, int window, int kv_format, int cap, int vocab,
+                       int logits_dtype, int32_t* ctx_len, void* k_cache, void* v_cache,
+                       const void* q, const void* tree_k, const void* tree_v,
+                       const int32_t* parent, const int32_t* tokens, const void* logits,
+                       float scale, float* out, float* lse, int32_t* argmax, int32_t* accept_len,
+                       int32_t* path, int32_t* out_tokens, void* workspace, size_t ws_bytes,
+                       uint32_t* status, cudaStream_t stream) {
+  if (kv_format != DFV_KV_Q4_0) return DFV_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return DFV_ERR_UNSUPPORTED;
+  if (with_accept && logits_dtype != DFV_DTYPE_F32 && logits_dtype != DFV_DTYPE_BF16)
+    return DFV_ERR_UNSUPPORTED;
+  StepPlan pl;
+  if (!step_plan(n_nodes, hq, hkv, head_dim, window, cap, vocab,
+                 with_accept ? logits_dtype : DFV_DTYPE_F32, with_accept, &pl))
+    return DFV_ERR_INVALID;
+  if (!ctx_len || !k_cache || !v_cache || !q || !tree_k || !tree_v || !parent || !out || !workspace)
+    return DFV_ERR_INVALID;
+  if (with_accept && (!tokens || !logits || !argmax || !accept_len || !path || !out_tokens))
+    return DFV_ERR_INVALID;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(tree_k, 16) ||
+      !aligned(tree_v, 16) || !aligned(out, 16) || !aligned(workspace, 256) ||
+      (with_accept && !aligned(logits, 16)))
+    return DFV_ERR_INVALID;
+  if (ws_bytes < pl.ws_total) return DFV_ERR_WORKSPACE;
+  StepParams p;
+  p.n_nodes = n_nodes;
+  p.max_depth = max_depth;
+  p.hq = hq;
+  p.hkv = hkv;
+  p.group = hq / hkv;
+  p.window = window;
+  p.capacity = cap;
+  p.vocab = vocab;
+  p.logits_dtype = logits_dtype;
+  p.rows = pl.rows;
+  p.n_mt = pl.n_mt;
+  p.splits = pl.splits;
+  p.units = pl.units;
+  p.lunits = pl.lunits;
+  p.lchunks = pl.lchunks;
+  p.lchunk_len = pl.lchunk_len;
+  p.lbulk = pl.lbulk;
+  p.do_accept = with_accept ? 1 : 0;
+  const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(head_dim));
+  p.scale_log2 = sc * 1.4426950408889634f;
+  p.ctx_len = ctx_len;
+  p.k_cache = static_cast<uint8_t*>(k_cache);
+  p.v_cache = static_cast<uint8_t*>(v_cache);
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.tree_k = static_cast<const __nv_bfloat16*>(tree_k);
+  p.tree_v = static_cast<const __nv_bfloat16*>(tree_v);
+  p.parent = parent;
+  p.tokens = tokens;
+  p.logits = logits;
+  p.out = out;
+  p.lse = lse;
+  p.argmax = argmax;
+  p.accept_len = accept_len;
+  p.path = path;
+  p.out_tokens = out_tokens;
+  char* ws = static_cast<char*>(workspace);
+  p.bar = reinterpret_cast<unsigned int*>(ws + pl.ws_bar);
+  p.arg_part = reinterpret_cast<ArgPartial*>(ws + pl.ws_arg);
+  p.qrows = reinterpret_cast<uint8_t*>(ws + pl.ws_qrows);
+  p.part_ml = reinterpret_cast<float2*>(ws + pl.ws_ml);
+  p.part_o = reinterpret_cast<__half*>(ws + pl.ws_o);
+  p.status = status;
+  switch (head_dim) {
+    case 64: return step_launch_d<64>(p, pl, stream);
+    case 128: return step_launch_d<128>(p, pl, stream);
+    default: return step_launch_d<256>(p, pl, stream);
+  }
+}
+
+}  // namespace dfv

@@ -1,0 +1,171 @@
+// 5th-generation tensor core (tcgen05) helpers for sm_103a: TMEM
+// allocation, shared-memory matrix descriptors for the 128-byte-swizzled
+// K-major layout, the f16 instruction descriptor, MMA issue / commit, and
+// TMEM loads. Hand-written inline PTX.
+#pragma once
+
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace dfv {
+namespace tc {
+
+// ---------------------------------------------------------------- TMEM
+
+// Allocate `ncols` TMEM columns (power of two >= 32); one full warp calls
+// this; the base address is written to *dst_smem.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- descriptors
+
+// Shared-memory matrix descriptor, K-major, 128-byte swizzle. `addr` is the
+// shared address of the first 16-byte chunk to read (atoms 1024-byte
+// aligned); 8-row groups are `sbo` bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);          // start address
+  d |= static_cast<uint64_t>(1u) << 16;                        // leading byte offset (unused)
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;      // stride byte offset
+  d |= static_cast<uint64_t>(1u) << 46;                        // descriptor version
+  d |= static_cast<uint64_t>(2u) << 61;                        // 128-byte swizzle
+  return d;
+}
+
+// Same, with an explicit leading byte offset: for an MN-major operand the
+// 64-element blocks along MN are `lbo` bytes apart and the 8-row groups
+// along K are `sbo` bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = smem_desc_sw128(addr, sbo);
+  d &= ~(static_cast<uint64_t>(0x3FFFu) << 16);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B, f32 accumulator, both
+// operands K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major = false) {
+  return (1u << 4)                                   // D format f32
+         | (0u << 7) | (0u << 10)                    // A, B format f16
+         | (0u << 15)                                // A K-major
+         | ((b_mn_major ? 1u : 0u) << 16)            // B K- or MN-major
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+// 2^x on the SFU (ex2.approx, subnormal results flushed to zero).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, one instruction of K = 16.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every MMA issued so far by this thread has completed.
+__device__ __forceinline__ void commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// ---------------------------------------------------------------- TMEM loads
+
+// 32 consecutive 32-bit columns of this thread's TMEM lane (32x32b shape).
+// The load and its wait are one asm statement: the destination registers
+// are written asynchronously, so no instruction may touch them in between.
+__device__ __forceinline__ void ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 32 consecutive 32-bit columns stored to this thread's TMEM lane; the
+// store's wait is in the same asm statement (its source registers stay live).
+__device__ __forceinline__ void st32(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+
+__device__ __forceinline__ void wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- swizzled layout
+
+// Byte offset of 16-byte chunk `c` (along K) of row `r` in a K-major,
+// 128-byte-swizzled tile of 16-bit elements with K = kcols elements: the
+// tile is stored as K/64 blocks of [rows x 128 B]; inside a block, row r is
+// at (r / 8) * 1024 + (r % 8) * 128 and chunk j of the row at ((j ^ (r % 8))
+// * 16).
+__device__ __forceinline__ uint32_t sw128_offset(int r, int c, int rows) {
+  const int kb = c >> 3, j = c & 7;
+  return static_cast<uint32_t>(kb * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 +
+                               ((j ^ (r & 7)) << 4));
+}
+
+}  // namespace tc
+}  // namespace dfv
