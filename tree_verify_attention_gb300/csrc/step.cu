@@ -52,6 +52,7 @@ constexpr float kRescaleLog2 = 8.0f;
 
 struct StepPlan {
   int rows, n_mt, splits, units, grid, lunits, lchunks, lchunk_len, lbulk, smem;
+  int walker, walker_local;
   size_t ws_bar, ws_arg, ws_qrows, ws_ml, ws_o, ws_total;
 };
 
@@ -59,6 +60,8 @@ struct StepParams {
   int n_nodes, max_depth, hq, hkv, group, window, capacity, vocab, logits_dtype;
   int rows, n_mt, splits, units, lunits, lchunks, lchunk_len, lbulk;
   int do_accept;
+  int walker;        // CTA that merges the argmax partials, walks and commits
+  int walker_local;  // 1: it quantises the tree rows into its own smem
   float scale_log2;
   int32_t* ctx_len;
   uint8_t* k_cache;
@@ -160,6 +163,20 @@ __device__ bool grid_barrier(unsigned int* bar, unsigned int nblocks, uint32_t* 
   return s_gok != 0;
 }
 
+// Maximum of a float over the CTA, returned to every thread.
+__device__ __forceinline__ float block_max(float v) {
+  __shared__ float sm[kStepThreads / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0) sm[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float m = sm[0];
+#pragma unroll
+  for (int w = 1; w < kStepThreads / 32; ++w) m = fmaxf(m, sm[w]);
+  __syncthreads();
+  return m;
+}
+
 // Thread 0 waits for an mbarrier phase; the CTA learns the outcome.
 __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int* s_flag,
                                          uint32_t* status) {
@@ -197,6 +214,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
   __shared__ float s_pmax[2][kRowsPerTile];
   __shared__ float s_m[kRowsPerTile], s_l[2][kRowsPerTile];
   __shared__ int s_ok, s_C;
+  __shared__ int s_wpar[kMaxNodes], s_wtok[kMaxNodes];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = gridDim.x, blk = blockIdx.x;
@@ -286,9 +304,61 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
     tc::tmem_alloc(s_tmem, kTmemCols);
     tc::fence_before_sync();
   }
-  int my_parent = -1;
-  if (unit >= 0 && tid < N) my_parent = tid == 0 ? -1 : p.parent[tid];
-  __syncthreads();   // barriers initialised
+  // ---- tree: depth and ancestor-or-self masks, by pointer jumping in one
+  // warp while the copies are in flight; ceil(log2 N) rounds cover every
+  // depth (< N)
+  if (unit >= 0 && warp == 0) {
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      const int n = lane + 32 * k;
+      if (n < N) {
+        int pa = n == 0 ? -1 : p.parent[n];
+        if (n > 0 && (pa < 0 || pa >= n)) {
+          if (blk == 0) report(p.status, DFV_DEV_BAD_TREE);
+          pa = 0;
+        }
+        s_J[n] = pa;
+        s_dep[n] = n > 0 ? 1 : 0;
+#pragma unroll
+        for (int w = 0; w < kMaskWords; ++w) s_anc[n][w] = (n >> 5) == w ? (1u << (n & 31)) : 0u;
+      }
+    }
+    int rounds = 0;
+    while ((1 << rounds) < N) ++rounds;
+    __syncwarp();
+#pragma unroll 1
+    for (int round = 0; round < rounds; ++round) {
+      int jj[3], nd[3], nj[3];
+      uint32_t nm[3][kMaskWords];
+#pragma unroll
+      for (int k = 0; k < 3; ++k) {
+        const int n = lane + 32 * k;
+        jj[k] = -1;
+        if (n < N) {
+          jj[k] = s_J[n];
+          if (jj[k] >= 0) {
+            nd[k] = s_dep[n] + s_dep[jj[k]];
+            nj[k] = s_J[jj[k]];
+#pragma unroll
+            for (int w = 0; w < kMaskWords; ++w) nm[k][w] = s_anc[n][w] | s_anc[jj[k]][w];
+          }
+        }
+      }
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < 3; ++k) {
+        const int n = lane + 32 * k;
+        if (n < N && jj[k] >= 0) {
+          s_dep[n] = nd[k];
+          s_J[n] = nj[k];
+#pragma unroll
+          for (int w = 0; w < kMaskWords; ++w) s_anc[n][w] = nm[k][w];
+        }
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();   // barriers initialised, tree bookkeeping done
 
   // ---- logits slice -> argmax partial
   if (p.do_accept) {
@@ -306,8 +376,28 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
         const int nvec = end > begin ? (end - begin) * esz / 16 : 0;
         const uint4* sv = reinterpret_cast<const uint4*>(sQ);
         if (esz == 2) {
-          for (int v = tid; v < nvec; v += kStepThreads)
-            scan_vec<__nv_bfloat16>(sv[v], begin + v * 8, best, bidx);
+          // pass 1: the slice maximum with packed bf16x2 max; pass 2: the
+          // lowest index holding it (IEEE equality: -0 == +0)
+          __nv_bfloat162 m2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+          for (int v = tid; v < nvec; v += kStepThreads) {
+            const uint4 x = sv[v];
+            const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&x);
+            m2 = __hmax2(m2, __hmax2(__hmax2(b[0], b[1]), __hmax2(b[2], b[3])));
+          }
+          const float mloc = fmaxf(__low2float(m2), __high2float(m2));
+          const float mx = block_max(mloc);
+          const __nv_bfloat162 mm = __floats2bfloat162_rn(mx, mx);
+          for (int v = tid; v < nvec && bidx == INT_MAX; v += kStepThreads) {
+            const uint4 x = sv[v];
+            const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+            for (int e = 0; e < 4 && bidx == INT_MAX; ++e) {
+              const unsigned msk = __heq2_mask(b[e], mm);
+              if (msk & 0xFFFFu) bidx = begin + v * 8 + 2 * e;
+              else if (msk & 0xFFFF0000u) bidx = begin + v * 8 + 2 * e + 1;
+            }
+          }
+          best = bidx == INT_MAX ? -INFINITY : mx;
         } else {
           for (int v = tid; v < nvec; v += kStepThreads)
             scan_vec<float>(sv[v], begin + v * 4, best, bidx);
@@ -327,14 +417,22 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
       }
       __syncthreads();   // the slice buffer is reused
     }
-    // ---- pre-quantise tree rows, on the CTAs without an attention unit
-    // when there are any, else spread over all CTAs
+    // ---- the walker keeps the tree's parents and tokens in smem
+    if (blk == p.walker && tid < N) {
+      s_wpar[tid] = p.parent[tid];
+      s_wtok[tid] = p.tokens[tid];
+    }
+    // ---- pre-quantise tree rows: into the walker's own smem when it has no
+    // attention unit and they fit, else into the workspace, spread over all
+    // CTAs
     const int tot = N * p.hkv * 2 * NB;
-    const int q0 = G > p.units ? p.units : 0;
-    const int nq = G - q0;
-    if (blk >= q0) {
-      const int b0 = static_cast<int>(static_cast<long>(blk - q0) * tot / nq);
-      const int b1 = static_cast<int>(static_cast<long>(blk - q0 + 1) * tot / nq);
+    uint8_t* qdst = p.walker_local ? sK : p.qrows;
+    const bool mine = p.walker_local ? blk == p.walker : true;
+    if (mine) {
+      const int nq = p.walker_local ? 1 : G;
+      const int bq = p.walker_local ? 0 : blk;
+      const int b0 = static_cast<int>(static_cast<long>(bq) * tot / nq);
+      const int b1 = static_cast<int>(static_cast<long>(bq + 1) * tot / nq);
       for (int it = b0 + tid; it < b1; it += kStepThreads) {
         const int b = it % NB;
         const int kv = (it / NB) & 1;
@@ -356,52 +454,13 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
             x[u4 * 8 + 2 * e + 1] = f.y;
           }
         }
-        q4_0_quantize_block(x, p.qrows + ((static_cast<size_t>(t) * p.hkv + hh) * 2 + kv) * L::kRowB +
+        q4_0_quantize_block(x, qdst + ((static_cast<size_t>(t) * p.hkv + hh) * 2 + kv) * L::kRowB +
                                    b * 18);
       }
     }
   }
 
   if (unit >= 0) {
-    // ---- tree: depth and ancestor-or-self masks by pointer jumping;
-    // ceil(log2 N) rounds cover every depth (< N)
-    if (tid < N) {
-      int pa = my_parent;
-      if (tid > 0 && (pa < 0 || pa >= tid)) {
-        if (blk == 0) report(p.status, DFV_DEV_BAD_TREE);
-        pa = 0;
-      }
-      s_J[tid] = pa;
-      s_dep[tid] = tid > 0 ? 1 : 0;
-#pragma unroll
-      for (int w = 0; w < kMaskWords; ++w)
-        s_anc[tid][w] = (tid >> 5) == w ? (1u << (tid & 31)) : 0u;
-    }
-    int rounds = 0;
-    while ((1 << rounds) < N) ++rounds;
-    __syncthreads();
-#pragma unroll 1
-    for (int round = 0; round < rounds; ++round) {
-      int j = -1, nd = 0, nj = -1;
-      uint32_t nm[kMaskWords];
-      if (tid < N) {
-        j = s_J[tid];
-        if (j >= 0) {
-          nd = s_dep[tid] + s_dep[j];
-          nj = s_J[j];
-#pragma unroll
-          for (int w = 0; w < kMaskWords; ++w) nm[w] = s_anc[tid][w] | s_anc[j][w];
-        }
-      }
-      __syncthreads();
-      if (tid < N && j >= 0) {
-        s_dep[tid] = nd;
-        s_J[tid] = nj;
-#pragma unroll
-        for (int w = 0; w < kMaskWords; ++w) s_anc[tid][w] = nm[w];
-      }
-      __syncthreads();
-    }
     if (blk == 0 && tid < N && s_dep[tid] > p.max_depth) report(p.status, DFV_DEV_DEPTH);
     if (tid < kRowsPerTile) {
       const int rg = mt * kRowsPerTile + tid;
@@ -418,14 +477,24 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
     const bool q_ok = cta_wait(bar_q, 0, &s_ok, p.status);
     if (q_ok) {
       constexpr int QU = kRowsPerTile * (D / 8) / kStepThreads;
+      constexpr int QB = QU < 4 ? QU : 4;
+#pragma unroll 1
+      for (int u0 = 0; u0 < QU; u0 += QB) {
+        uint4 qv[QB];
 #pragma unroll
-      for (int u = 0; u < QU; ++u) {
-        const int it = tid + u * kStepThreads;
-        const int lr = it / (D / 8), c = it % (D / 8);
-        const uint4 v = mt * kRowsPerTile + lr < p.rows
-                            ? *reinterpret_cast<const uint4*>(sV + lr * D * 2 + c * 16)
-                            : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(sQ + tc::sw128_offset(lr, c, kRowsPerTile)) = bf16x8_to_f16x8(v);
+        for (int u = 0; u < QB; ++u) {
+          const int it = tid + (u0 + u) * kStepThreads;
+          const int lr = it / (D / 8), c = it % (D / 8);
+          qv[u] = mt * kRowsPerTile + lr < p.rows
+                      ? *reinterpret_cast<const uint4*>(sV + lr * D * 2 + c * 16)
+                      : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < QB; ++u) {
+          const int it = tid + (u0 + u) * kStepThreads;
+          const int lr = it / (D / 8), c = it % (D / 8);
+          *reinterpret_cast<uint4*>(sQ + tc::sw128_offset(lr, c, kRowsPerTile)) = bf16x8_to_f16x8(qv[u]);
+        }
       }
     }
     __syncthreads();
@@ -459,16 +528,31 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
           const uint8_t* base;
           if constexpr (L::kBulk) base = kvi ? sK : sRawK;
           else base = (kvi ? p.v_cache : p.k_cache) + (static_cast<size_t>(h) * p.capacity + j0) * L::kRowB;
-          for (int it = tid; it < kChunk * NB; it += kStepThreads) {
-            const int key = it / NB, b = it % NB;
-            uint4 o4[4];
+          // each thread: kChunk * NB / kStepThreads blocks; all words are
+          // loaded first so the loads overlap
+          constexpr int BPT = kChunk * NB / kStepThreads;
+          constexpr int BB = BPT < 2 ? BPT : 2;
+#pragma unroll 1
+          for (int u0 = 0; u0 < BPT; u0 += BB) {
+            uint16_t w[BB][9];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o4[e] = make_uint4(0, 0, 0, 0);
-            if (key < nk)
-              q4_0_block_chunks(reinterpret_cast<const uint16_t*>(base + key * L::kRowB + b * 18), o4);
+            for (int u = 0; u < BB; ++u) {
+              const int it = tid + (u0 + u) * kStepThreads;
+              const int key = it / NB, b = it % NB;
+              const uint16_t* src = reinterpret_cast<const uint16_t*>(base + key * L::kRowB + b * 18);
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              *reinterpret_cast<uint4*>(dst + tc::sw128_offset(key, b * 4 + e, kChunk)) = o4[e];
+              for (int e = 0; e < 9; ++e) w[u][e] = key < nk ? src[e] : static_cast<uint16_t>(0);
+            }
+#pragma unroll
+            for (int u = 0; u < BB; ++u) {
+              const int it = tid + (u0 + u) * kStepThreads;
+              const int key = it / NB, b = it % NB;
+              uint4 o4[4];
+              q4_0_block_chunks(w[u], o4);   // an all-zero block dequantises to zeros
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                *reinterpret_cast<uint4*>(dst + tc::sw128_offset(key, b * 4 + e, kChunk)) = o4[e];
+            }
           }
           __syncthreads();   // raw V (in sK) consumed before K overwrites it
         }
@@ -569,6 +653,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
         l_half = l_half * alpha + rs;
         if (o_valid && __any_sync(0xffffffffu, rescale)) {
           // this warp's half of the row's O columns
+#pragma unroll 1
           for (int c = 0; c < D / 64; ++c) {
             const uint32_t col = static_cast<uint32_t>(hc * (D / 2) + c * 32);
             float ov[32];
@@ -619,22 +704,33 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
         for (int e = 0; e < 32; e += 4)
           *reinterpret_cast<float4*>(stage + lane * 36 + e) = make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
         __syncwarp();
+        // all shared loads first, then the global stores (generic pointers
+        // would otherwise serialise the loop)
+        float4 v[8];
+        float lsum8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int rr = i * 4 + (lane >> 3);             // row within the warp's 32
           const int row = (warp & 3) * 32 + rr;
+          v[i] = *reinterpret_cast<const float4*>(stage + rr * 36 + (lane & 7) * 4);
+          lsum8[i] = s_l[0][row] + s_l[1][row];
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = i * 4 + (lane >> 3);
+          const int row = (warp & 3) * 32 + rr;
           const int rg = mt * kRowsPerTile + row;
-          float4 v = *reinterpret_cast<const float4*>(stage + rr * 36 + (lane & 7) * 4);
-          const float l = s_l[0][row] + s_l[1][row];
+          const float l = lsum8[i];
           if (rg < p.rows && o_valid && alive && l > 0.f) {
-            const float inv = 1.f / l;
-            v.x *= inv; v.y *= inv; v.z *= inv; v.w *= inv;
+            const float inv = __frcp_rn(l);
+            float4 w = v[i];
+            w.x *= inv; w.y *= inv; w.z *= inv; w.w *= inv;
             if (p.splits == 1) {
               const int node = rg / p.group, qh = h * p.group + rg % p.group;
               *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(node) * p.hq + qh) * D + col +
-                                         (lane & 7) * 4) = v;
+                                         (lane & 7) * 4) = w;
             } else {
-              __half2 h01 = __floats2half2_rn(v.x, v.y), h23 = __floats2half2_rn(v.z, v.w);
+              __half2 h01 = __floats2half2_rn(w.x, w.y), h23 = __floats2half2_rn(w.z, w.w);
               uint2 hv;
               hv.x = *reinterpret_cast<uint32_t*>(&h01);
               hv.y = *reinterpret_cast<uint32_t*>(&h23);
@@ -670,20 +766,23 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
   // ---- merge the key splits of a slice of the output rows (CTA 0 is kept
   // free for the walk when the step has one)
   if (p.splits > 1) {
-    const int c0b = (p.do_accept && G > 1) ? 1 : 0;
-    const int nb = G - c0b;
+    // CTA index among the merging CTAs (all but the walker)
+    const bool skip = p.do_accept && G > 1 && blk == p.walker;
+    const int nb = (p.do_accept && G > 1) ? G - 1 : G;
+    const int mb = (p.do_accept && G > 1 && blk > p.walker) ? blk - 1 : blk;
     const int total = p.hkv * p.rows;
-    if (blk >= c0b) {
-      const int r0 = static_cast<int>(static_cast<long>(blk - c0b) * total / nb);
-      const int r1 = static_cast<int>(static_cast<long>(blk - c0b + 1) * total / nb);
+    if (!skip) {
+      const int r0 = static_cast<int>(static_cast<long>(mb) * total / nb);
+      const int r1 = static_cast<int>(static_cast<long>(mb + 1) * total / nb);
       for (int it = tid; it < (r1 - r0) * (D / 4); it += kStepThreads) {
         const int gr = r0 + it / (D / 4), d = (it % (D / 4)) * 4;
         const int hh = gr / p.rows, rg = gr % p.rows;
         const int mtt = rg / kRowsPerTile, rr = rg % kRowsPerTile;
         const size_t ubase = static_cast<size_t>(hh * p.n_mt + mtt) * p.splits;
-        constexpr int SB = 24;
+        constexpr int SB = 8;
         float M = -INFINITY, lsum = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
         for (int s0 = 0; s0 < p.splits; s0 += SB) {
           float2 ml[SB];
           uint2 ov[SB];
@@ -728,8 +827,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
     }
   }
 
-  // ---- CTA 0: argmax merge, walk, commit
-  if (p.do_accept && blk == 0) {
+  // ---- the walker: argmax merge, walk, commit
+  if (p.do_accept && blk == p.walker) {
     __shared__ int s_am[kMaxNodes];
     __shared__ int s_path[kMaxNodes];
     __shared__ int s_L;
@@ -757,10 +856,10 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
         par[s] = -2;
         tok[s] = 0;
         if (n >= 1 && n < N) {
-          int pa = p.parent[n];
+          int pa = s_wpar[n];
           if (pa < 0 || pa >= n) pa = 0;
           par[s] = pa;
-          tok[s] = p.tokens[n];
+          tok[s] = s_wtok[n];
         }
       }
       int cur = 0, Lw = 1;
@@ -783,7 +882,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
       for (int k = lane; k < N; k += 32) {
         p.path[k] = k < Lw ? s_path[k] : -1;
         int ot = -1;
-        if (k < Lw - 1) ot = p.tokens[s_path[k + 1]];
+        if (k < Lw - 1) ot = s_wtok[s_path[k + 1]];
         else if (k == Lw - 1) ot = s_am[s_path[Lw - 1]];
         p.out_tokens[k] = ot;
       }
@@ -804,11 +903,11 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
         const int kv = (it / W4) & 1;
         const int hh = (it / (2 * W4)) % p.hkv;
         const int k = it / (2 * W4 * p.hkv);
-        const uint32_t* src = reinterpret_cast<const uint32_t*>(
-            p.qrows + ((static_cast<size_t>(s_path[k]) * p.hkv + hh) * 2 + kv) * L::kRowB);
+        const size_t so = ((static_cast<size_t>(s_path[k]) * p.hkv + hh) * 2 + kv) * L::kRowB;
         uint32_t* dst = reinterpret_cast<uint32_t*>(
             (kv ? p.v_cache : p.k_cache) + (static_cast<size_t>(hh) * p.capacity + Cc + k) * L::kRowB);
-        dst[w] = __ldcg(src + w);
+        dst[w] = p.walker_local ? reinterpret_cast<const uint32_t*>(sK + so)[w]
+                                : __ldcg(reinterpret_cast<const uint32_t*>(p.qrows + so) + w);
       }
       __syncthreads();
       if (tid == 0) *p.ctx_len = Cc + Lc;
@@ -858,6 +957,14 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
     pl->lbulk = (static_cast<long>(vocab) * esz % 16 == 0) && pl->lchunk_len * esz <= tile_b;
   } else {
     pl->lchunks = pl->lunits = pl->lchunk_len = pl->lbulk = 0;
+  }
+  // the walker: a CTA without an attention unit when there is one
+  pl->walker = with_accept ? (pl->grid > pl->units ? pl->grid - 1 : 0) : -1;
+  {
+    const long qbytes = static_cast<long>(n_nodes) * hkv * 2 * (head_dim / 32 * 18);
+    const long room = static_cast<long>(kChunk) * (head_dim > kChunk ? head_dim : kChunk) * 2 +
+                      static_cast<long>(kRowsPerTile) * head_dim * 2;   // sK + sV regions
+    pl->walker_local = with_accept && pl->grid > pl->units && qbytes <= room ? 1 : 0;
   }
   switch (head_dim) {
     case 64: pl->smem = StepSmem<64>::kBytes; break;
@@ -959,6 +1066,8 @@ dfv_status step_launch(bool with_accept, int n_nodes, int max_depth, int hq, int
   p.lchunk_len = pl.lchunk_len;
   p.lbulk = pl.lbulk;
   p.do_accept = with_accept ? 1 : 0;
+  p.walker = pl.walker;
+  p.walker_local = pl.walker_local;
   const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(head_dim));
   p.scale_log2 = sc * 1.4426950408889634f;
   p.ctx_len = ctx_len;
