@@ -49,10 +49,11 @@ constexpr int kChunk = 128;         // keys per chunk (UMMA N of S, K of P V)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxStepSplits = 256;
 constexpr float kRescaleLog2 = 8.0f;
+constexpr int kLogitVecs = 16;      // 16-byte logits vectors a thread keeps in flight
 
 struct StepPlan {
   int rows, n_mt, splits, units, grid, lunits, lchunks, lchunk_len, lbulk, smem;
-  int walker, walker_local;
+  int walker, walker_local, lbase, lcount;
   size_t ws_bar, ws_arg, ws_qrows, ws_ml, ws_o, ws_total;
 };
 
@@ -60,6 +61,7 @@ struct StepParams {
   int n_nodes, max_depth, hq, hkv, group, window, capacity, vocab, logits_dtype;
   int rows, n_mt, splits, units, lunits, lchunks, lchunk_len, lbulk;
   int do_accept;
+  int lbase, lcount;  // CTAs [lbase, lbase + lcount) stream the logits
   int walker;        // CTA that merges the argmax partials, walks and commits
   int walker_local;  // 1: it quantises the tree rows into its own smem
   float scale_log2;
@@ -206,7 +208,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
   uint64_t* bar_mma = bar_kv + 1;
   uint64_t* bar_lg = bar_kv + 2;
   uint64_t* bar_q = bar_kv + 3;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_kv + 4);
+  uint64_t* bar_lg1 = bar_kv + 4;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_kv + 5);
 
   __shared__ int s_J[kMaxNodes], s_dep[kMaxNodes];
   __shared__ uint32_t s_anc[kMaxNodes][kMaskWords];
@@ -252,18 +255,97 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
     bulk_g2s(sRawK, p.k_cache + off, bytes, bar_kv);
     bulk_g2s(sK, p.v_cache + off, bytes, bar_kv);
   };
-  auto issue_logits = [&](int u) {
+  auto issue_logits = [&](int u, uint8_t* buf, uint64_t* bar) {
     const int node = u / p.lchunks, ch = u % p.lchunks;
     const int begin = ch * p.lchunk_len;
     const int end = min(p.vocab, begin + p.lchunk_len);
     const uint32_t bytes = end > begin ? static_cast<uint32_t>((end - begin) * esz) : 0u;
     fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar_lg, bytes);
+    mbar_arrive_expect_tx(bar, bytes);
     if (bytes)
-      bulk_g2s(sQ, static_cast<const uint8_t*>(p.logits) +
-                       (static_cast<size_t>(node) * p.vocab + begin) * esz,
-               bytes, bar_lg);
+      bulk_g2s(buf, static_cast<const uint8_t*>(p.logits) +
+                        (static_cast<size_t>(node) * p.vocab + begin) * esz,
+               bytes, bar);
   };
+  // the logits slice of this CTA (unit blk): 16-byte vectors loaded into
+  // registers at the start and scanned later (attention CTAs scan while
+  // their first MMA runs); slices beyond one per CTA use plain loads
+  const bool lhas = p.do_accept && blk < p.lunits;
+  const bool lreg = lhas && p.lbulk;
+  uint4 lg[kLogitVecs];
+  int lbegin = 0, lnvec = 0;
+  if (lreg) {
+    const int node = blk / p.lchunks, ch = blk % p.lchunks;
+    lbegin = ch * p.lchunk_len;
+    const int lend = min(p.vocab, lbegin + p.lchunk_len);
+    lnvec = lend > lbegin ? (lend - lbegin) * esz / 16 : 0;
+    const uint4* vp = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.logits) +
+                                                     (static_cast<size_t>(node) * p.vocab + lbegin) * esz);
+#pragma unroll
+    for (int u = 0; u < kLogitVecs; ++u) {
+      const int v = tid + u * kStepThreads;
+      lg[u] = v < lnvec ? __ldcs(vp + v) : make_uint4(0, 0, 0, 0);
+    }
+  }
+  auto scan_logits = [&]() {
+    // the thread's maximum over independent chains, then the lowest index
+    // holding it (min over independent chains); (max, lowest index) pairs
+    // then merge across the CTA
+    float best = -INFINITY;
+    if (esz == 2) {
+      __nv_bfloat162 m2[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) m2[e] = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+#pragma unroll
+      for (int u = 0; u < kLogitVecs; ++u) {
+        if (tid + u * kStepThreads < lnvec) {
+          const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&lg[u]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) m2[e] = __hmax2(m2[e], b[e]);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) best = fmaxf(best, fmaxf(__low2float(m2[e]), __high2float(m2[e])));
+    } else {
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int u = 0; u < kLogitVecs; ++u) {
+        if (tid + u * kStepThreads < lnvec) {
+          const float* f = reinterpret_cast<const float*>(&lg[u]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) m4[e] = fmaxf(m4[e], f[e]);
+        }
+      }
+      best = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+    }
+    int i4[4] = {INT_MAX, INT_MAX, INT_MAX, INT_MAX};
+#pragma unroll
+    for (int u = 0; u < kLogitVecs; ++u) {
+      const int v = tid + u * kStepThreads;
+      if (v < lnvec) {
+        if (esz == 2) {
+          const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&lg[u]);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (__bfloat162float(b[e]) == best) i4[e & 3] = min(i4[e & 3], lbegin + v * 8 + e);
+        } else {
+          const float* f = reinterpret_cast<const float*>(&lg[u]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (f[e] == best) i4[e] = min(i4[e], lbegin + v * 4 + e);
+        }
+      }
+    }
+    int bidx = min(min(i4[0], i4[1]), min(i4[2], i4[3]));
+    if (bidx == INT_MAX) best = -INFINITY;   // no element: loses every merge
+    block_argmax(best, bidx);
+    if (tid == 0) {
+      p.arg_part[blk].v = best;
+      p.arg_part[blk].idx = bidx;
+    }
+    __syncthreads();
+  };
+  bool lscanned = !lreg;
 
   // ================================================================ phase A
   if (tid == 0) {
@@ -271,8 +353,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
     mbar_init(bar_mma, 1);
     mbar_init(bar_lg, 1);
     mbar_init(bar_q, 1);
+    mbar_init(bar_lg1, 1);
     fence_mbar_init();
-    if (p.do_accept && p.lbulk && blk < p.lunits) issue_logits(blk);
     if (unit >= 0) {
       // bf16 Q rows of the tile -> sV (row-major staging), one copy per
       // node run of consecutive query heads
@@ -360,62 +442,32 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
   }
   __syncthreads();   // barriers initialised, tree bookkeeping done
 
-  // ---- logits slice -> argmax partial
+  // ---- logits: CTAs without an attention unit scan their slice now; slices
+  // beyond one per CTA (or unaligned rows) go through plain loads
   if (p.do_accept) {
-    uint32_t ph_lg = 0;
-    for (int u = blk; u < p.lunits; u += G) {
+    if (unit < 0 && lreg) {
+      scan_logits();
+      lscanned = true;
+    }
+    for (int u = lreg ? blk + G : blk; u < p.lunits; u += G) {
       const int node = u / p.lchunks, ch = u % p.lchunks;
       const int begin = ch * p.lchunk_len;
       const int end = min(p.vocab, begin + p.lchunk_len);
       float best = -INFINITY;
       int bidx = INT_MAX;
-      if (p.lbulk) {
-        if (u != blk && tid == 0) issue_logits(u);
-        if (!cta_wait(bar_lg, ph_lg, &s_ok, p.status)) break;
-        ph_lg ^= 1u;
-        const int nvec = end > begin ? (end - begin) * esz / 16 : 0;
-        const uint4* sv = reinterpret_cast<const uint4*>(sQ);
-        if (esz == 2) {
-          // pass 1: the slice maximum with packed bf16x2 max; pass 2: the
-          // lowest index holding it (IEEE equality: -0 == +0)
-          __nv_bfloat162 m2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
-          for (int v = tid; v < nvec; v += kStepThreads) {
-            const uint4 x = sv[v];
-            const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&x);
-            m2 = __hmax2(m2, __hmax2(__hmax2(b[0], b[1]), __hmax2(b[2], b[3])));
-          }
-          const float mloc = fmaxf(__low2float(m2), __high2float(m2));
-          const float mx = block_max(mloc);
-          const __nv_bfloat162 mm = __floats2bfloat162_rn(mx, mx);
-          for (int v = tid; v < nvec && bidx == INT_MAX; v += kStepThreads) {
-            const uint4 x = sv[v];
-            const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&x);
-#pragma unroll
-            for (int e = 0; e < 4 && bidx == INT_MAX; ++e) {
-              const unsigned msk = __heq2_mask(b[e], mm);
-              if (msk & 0xFFFFu) bidx = begin + v * 8 + 2 * e;
-              else if (msk & 0xFFFF0000u) bidx = begin + v * 8 + 2 * e + 1;
-            }
-          }
-          best = bidx == INT_MAX ? -INFINITY : mx;
-        } else {
-          for (int v = tid; v < nvec; v += kStepThreads)
-            scan_vec<float>(sv[v], begin + v * 4, best, bidx);
-        }
-      } else if (esz == 2) {
+      if (esz == 2)
         chunk_argmax<__nv_bfloat16, 16>(
             static_cast<const __nv_bfloat16*>(p.logits) + static_cast<size_t>(node) * p.vocab,
             begin, end, best, bidx);
-      } else {
+      else
         chunk_argmax<float, 16>(static_cast<const float*>(p.logits) + static_cast<size_t>(node) * p.vocab,
                                 begin, end, best, bidx);
-      }
       block_argmax(best, bidx);
       if (tid == 0) {
         p.arg_part[u].v = best;
         p.arg_part[u].idx = bidx;
       }
-      __syncthreads();   // the slice buffer is reused
+      __syncthreads();
     }
     // ---- the walker keeps the tree's parents and tokens in smem
     if (blk == p.walker && tid < N) {
@@ -557,17 +609,44 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
           __syncthreads();   // raw V (in sK) consumed before K overwrites it
         }
       } else {
-        // tree chunk: keys t = 0..N-1 from tree_k / tree_v (bf16 -> fp16)
+        // tree chunk: keys t = 0..N-1 from tree_k / tree_v (bf16 -> fp16);
+        // the other key rows are zero. The loads of a thread are issued
+        // together.
         const int t0 = (cc - n_cc) * kChunk;
-        for (int it = tid; it < 2 * kChunk * (D / 8); it += kStepThreads) {
-          const int kvi = it / (kChunk * (D / 8));
-          const int key = (it / (D / 8)) % kChunk, c = it % (D / 8);
-          const int t = t0 + key;
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (t < N)
-            v = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(
-                (kvi ? p.tree_v : p.tree_k) + (static_cast<size_t>(t) * p.hkv + h) * D + c * 8));
-          *reinterpret_cast<uint4*>((kvi ? sV : sK) + tc::sw128_offset(key, c, kChunk)) = v;
+        const int nt = max(0, min(kChunk, N - t0));             // real keys here
+        const int real = 2 * nt * (D / 8);                      // 16-byte items with data
+        constexpr int TB = 8;
+#pragma unroll 1
+        for (int it0 = tid; it0 < real; it0 += TB * kStepThreads) {
+          uint4 v[TB];
+#pragma unroll
+          for (int u = 0; u < TB; ++u) {
+            const int it = it0 + u * kStepThreads;
+            v[u] = make_uint4(0, 0, 0, 0);
+            if (it < real) {
+              const int kvi = it / (nt * (D / 8));
+              const int key = (it / (D / 8)) % nt, c = it % (D / 8);
+              v[u] = *reinterpret_cast<const uint4*>(
+                  (kvi ? p.tree_v : p.tree_k) + (static_cast<size_t>(t0 + key) * p.hkv + h) * D + c * 8);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < TB; ++u) {
+            const int it = it0 + u * kStepThreads;
+            if (it < real) {
+              const int kvi = it / (nt * (D / 8));
+              const int key = (it / (D / 8)) % nt, c = it % (D / 8);
+              *reinterpret_cast<uint4*>((kvi ? sV : sK) + tc::sw128_offset(key, c, kChunk)) =
+                  bf16x8_to_f16x8(v[u]);
+            }
+          }
+        }
+        const int zero = 2 * (kChunk - nt) * (D / 8);
+        for (int it = tid; it < zero; it += kStepThreads) {
+          const int kvi = it / ((kChunk - nt) * (D / 8));
+          const int key = nt + (it / (D / 8)) % (kChunk - nt), c = it % (D / 8);
+          *reinterpret_cast<uint4*>((kvi ? sV : sK) + tc::sw128_offset(key, c, kChunk)) =
+              make_uint4(0, 0, 0, 0);
         }
       }
       fence_proxy_async_smem();
@@ -584,6 +663,10 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
                       tc::smem_desc_sw128(smem_u32(sK) + off, 1024), idesc, kk > 0 ? 1u : 0u);
         }
         tc::commit(bar_mma);
+      }
+      if (!lscanned) {          // the logits slice, while the MMA runs
+        scan_logits();
+        lscanned = true;
       }
       if (!cta_wait(bar_mma, ph_mma, &s_ok, p.status)) { alive = false; break; }
       ph_mma ^= 1u;
@@ -636,7 +719,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
           m_run = cmax;
         }
         const float sub = m_run == -INFINITY ? 0.f : m_run;
-        float rs = 0.f;
+        float rs4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           uint32_t w4[4];
@@ -644,13 +727,13 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
           for (int e = 0; e < 4; ++e) {
             const float p0 = tc::ex2(s[c * 8 + 2 * e] - sub);
             const float p1 = tc::ex2(s[c * 8 + 2 * e + 1] - sub);
-            rs += p0 + p1;
+            rs4[e] += p0 + p1;
             w4[e] = pack_half2(p0, p1);
           }
           *reinterpret_cast<uint4*>(sK + tc::sw128_offset(r, hc * 8 + c, kRowsPerTile)) =
               make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
-        l_half = l_half * alpha + rs;
+        l_half = l_half * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
         if (o_valid && __any_sync(0xffffffffu, rescale)) {
           // this warp's half of the row's O columns
 #pragma unroll 1
@@ -688,6 +771,10 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
       tc::fence_after_sync();
     }
 
+    if (!lscanned) {
+      scan_logits();
+      lscanned = true;
+    }
     // ---- epilogue: O rows from TMEM -> workspace (or the output when
     // there is one split); 32 x 32 blocks go through smem (sQ is free) so
     // that global stores are row-contiguous
@@ -696,6 +783,15 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
     __syncthreads();
     {
       float* stage = reinterpret_cast<float*>(sQ) + warp * (32 * 36);
+      // 1 / l of the 8 rows this lane stores (rows 4 i + lane / 8)
+      float inv8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int row = (warp & 3) * 32 + i * 4 + (lane >> 3);
+        const float l = s_l[0][row] + s_l[1][row];
+        inv8[i] = l > 0.f ? __fdividef(1.f, l) : 0.f;
+      }
+#pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         const int col = hc * (D / 2) + c * 32;
         float ov[32];
@@ -707,22 +803,18 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
         // all shared loads first, then the global stores (generic pointers
         // would otherwise serialise the loop)
         float4 v[8];
-        float lsum8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int rr = i * 4 + (lane >> 3);             // row within the warp's 32
-          const int row = (warp & 3) * 32 + rr;
           v[i] = *reinterpret_cast<const float4*>(stage + rr * 36 + (lane & 7) * 4);
-          lsum8[i] = s_l[0][row] + s_l[1][row];
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int rr = i * 4 + (lane >> 3);
           const int row = (warp & 3) * 32 + rr;
           const int rg = mt * kRowsPerTile + row;
-          const float l = lsum8[i];
-          if (rg < p.rows && o_valid && alive && l > 0.f) {
-            const float inv = __frcp_rn(l);
+          if (rg < p.rows && o_valid && alive && inv8[i] > 0.f) {
+            const float inv = inv8[i];
             float4 w = v[i];
             w.x *= inv; w.y *= inv; w.z *= inv; w.w *= inv;
             if (p.splits == 1) {
@@ -832,14 +924,21 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
     __shared__ int s_am[kMaxNodes];
     __shared__ int s_path[kMaxNodes];
     __shared__ int s_L;
+    // every partial in one round of loads (staged in sQ), then per node
+    ArgPartial* s_ap = reinterpret_cast<ArgPartial*>(sQ);
+    for (int i = tid; i < p.lunits; i += kStepThreads) {
+      ArgPartial a;
+      a.v = __ldcg(&p.arg_part[i].v);
+      a.idx = __ldcg(&p.arg_part[i].idx);
+      s_ap[i] = a;
+    }
+    __syncthreads();
     for (int node = warp; node < N; node += kStepThreads / 32) {
       float best = -INFINITY;
       int bidx = INT_MAX;
       for (int c = lane; c < p.lchunks; c += 32) {
-        const ArgPartial* ap = p.arg_part + node * p.lchunks + c;
-        const float v = __ldcg(&ap->v);
-        const int i = __ldcg(&ap->idx);
-        if (beats(v, i, best, bidx)) { best = v; bidx = i; }
+        const ArgPartial a = s_ap[node * p.lchunks + c];
+        if (beats(a.v, a.idx, best, bidx)) { best = a.v; bidx = a.idx; }
       }
       warp_argmax(best, bidx);
       if (lane == 0) {
@@ -940,12 +1039,16 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
   pl->units = hkv * pl->n_mt * pl->splits;
   const int tile_b = kRowsPerTile * head_dim * 2;        // logits staging bytes
   const int esz = logits_dtype == DFV_DTYPE_BF16 ? 2 : 4;
+  // every CTA streams logits (one SM alone can only keep a few tens of KB
+  // in flight, so the stream needs all of them)
+  pl->lbase = 0;
+  pl->lcount = pl->grid;
   if (with_accept) {
-    // slices: one per CTA when they fit the staging area, more otherwise;
-    // bulk-copied when every slice starts and ends 16-byte aligned
+    // slices: at most one per CTA when they fit the registers of the CTA
+    // (kLogitVecs 16-byte vectors per thread), more otherwise
     int lc = sms / n_nodes;
     if (lc < 1) lc = 1;
-    const int per = tile_b / esz;
+    const int per = kLogitVecs * kStepThreads * 16 / esz;
     const int need = (vocab + per - 1) / per;
     if (lc < need) lc = need;
     const int cap_c = (vocab + 255) / 256;
@@ -954,7 +1057,8 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
     pl->lunits = n_nodes * lc;
     const int align_el = 16 / esz;
     pl->lchunk_len = (((vocab + lc - 1) / lc) + align_el - 1) / align_el * align_el;
-    pl->lbulk = (static_cast<long>(vocab) * esz % 16 == 0) && pl->lchunk_len * esz <= tile_b;
+    pl->lbulk = (static_cast<long>(vocab) * esz % 16 == 0) &&
+                pl->lchunk_len * esz <= kLogitVecs * kStepThreads * 16;
   } else {
     pl->lchunks = pl->lunits = pl->lchunk_len = pl->lbulk = 0;
   }
@@ -962,8 +1066,7 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
   pl->walker = with_accept ? (pl->grid > pl->units ? pl->grid - 1 : 0) : -1;
   {
     const long qbytes = static_cast<long>(n_nodes) * hkv * 2 * (head_dim / 32 * 18);
-    const long room = static_cast<long>(kChunk) * (head_dim > kChunk ? head_dim : kChunk) * 2 +
-                      static_cast<long>(kRowsPerTile) * head_dim * 2;   // sK + sV regions
+    const long room = static_cast<long>(kChunk) * (head_dim > kChunk ? head_dim : kChunk) * 2;  // sK
     pl->walker_local = with_accept && pl->grid > pl->units && qbytes <= room ? 1 : 0;
   }
   switch (head_dim) {
@@ -1068,6 +1171,8 @@ dfv_status step_launch(bool with_accept, int n_nodes, int max_depth, int hq, int
   p.do_accept = with_accept ? 1 : 0;
   p.walker = pl.walker;
   p.walker_local = pl.walker_local;
+  p.lbase = pl.lbase;
+  p.lcount = pl.lcount;
   const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(head_dim));
   p.scale_log2 = sc * 1.4426950408889634f;
   p.ctx_len = ctx_len;
