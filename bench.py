@@ -48,6 +48,7 @@ def parse_args(argv=None):
     ap.add_argument("--pool", type=int, default=POOL, help="distinct step inputs")
     ap.add_argument("--replicas", type=int, default=REPLICAS, help="KV-cache replicas")
     ap.add_argument("--cpu-child", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--source-hash", action="store_true", help="print the kernel source hash")
     return ap.parse_args(argv)
 
 
@@ -391,7 +392,7 @@ def run_gpu(args):
     }
     roof = {"kernel": "step_kernel<256>", "bound": "hbm",
             "achieved": (kv_b + lg_b) / t_kernel / 1e9, "peak": hbm, "unit": "GB/s",
-            "frac": (kv_b + lg_b) / t_kernel / 1e9 / hbm, "traffic": None,
+            "frac": (kv_b + lg_b) / t_kernel / 1e9 / hbm, "traffic": recorded_traffic(),
             "peak_source": peak_src + " copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
             "algorithmic_bytes": kv_b + lg_b,
             "tensor_tflops": flops / t_kernel / 1e12, "tensor_peak": tf}
@@ -431,6 +432,33 @@ def run_gpu(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def kernel_source_hash():
+    """Hash of the CUDA sources, to tell whether recorded ncu counters still
+    describe the kernel being timed."""
+    import hashlib
+    d = os.path.join(ROOT, "tree_verify_attention_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(f.encode())
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per step-kernel launch from the committed ncu summary, or
+    None when the kernel sources changed since it was taken."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "step_kernel_traffic.json")) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
 
 
 def _peaks():
@@ -505,6 +533,9 @@ def run_e2e(args, api, cfg, steps_np, caches, ctx_all, ctx0, st, stream, dev):
 
 def main(argv=None):
     args = parse_args(argv)
+    if args.source_hash:
+        print(kernel_source_hash())
+        return
     if args.cpu_child:
         cpu_oracle_child(args.cpu_seconds, args.steps)
         return
