@@ -451,14 +451,21 @@ def kernel_source_hash():
 def recorded_traffic():
     """DRAM bytes per step-kernel launch from the committed ncu summary, or
     None when the kernel sources changed since it was taken."""
+    rec = {}
     try:
-        with open(os.path.join(ROOT, "profiles", "step_kernel_traffic.json")) as f:
-            rec = json.load(f)
-    except (OSError, ValueError):
+        with open(os.path.join(ROOT, "profiles", "step_kernel_traffic.txt")) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    rec[k.strip()] = v.strip()
+    except OSError:
         return None
     if rec.get("source_hash") != kernel_source_hash():
         return None
-    return rec.get("dram_bytes_per_launch")
+    try:
+        return int(rec["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 def _peaks():
