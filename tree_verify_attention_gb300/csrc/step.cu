@@ -80,7 +80,9 @@ struct StepParams {
   int32_t* accept_len;
   int32_t* path;
   int32_t* out_tokens;
-  unsigned int* bar;        // [0] arrivals, [1] generation
+  unsigned int* bar;        // [2] CTAs done with ctx and their argmax partial
+                            // (the walker resets it); [4 + 2 g], [5 + 2 g]:
+                            // arrivals / generation of split group g
   ArgPartial* arg_part;     // [lunits]
   uint8_t* qrows;           // [N][Hkv][2][row bytes]
   float2* part_ml;          // [units][128]  (running max, log2 units; sum)
@@ -136,20 +138,21 @@ __device__ __forceinline__ void q4_0_block_chunks(const uint16_t* w, uint4* out)
   }
 }
 
-// Bounded grid-wide barrier of a cooperative launch; false on timeout.
-__device__ bool grid_barrier(unsigned int* bar, unsigned int nblocks, uint32_t* status) {
+// Bounded barrier among the `n` CTAs of one group (all co-resident in a
+// cooperative launch); false on timeout.
+__device__ bool group_barrier(unsigned int* cnt, unsigned int n, uint32_t* status) {
   __shared__ int s_gok;
   __syncthreads();
   if (threadIdx.x == 0) {
-    volatile unsigned int* vgen = bar + 1;
+    volatile unsigned int* vgen = cnt + 1;
     const unsigned int gen = *vgen;
     __threadfence();
-    const unsigned int arrived = atomicAdd(bar, 1u);
+    const unsigned int arrived = atomicAdd(cnt, 1u);
     int ok = 1;
-    if (arrived == nblocks - 1) {
-      atomicExch(bar, 0u);
+    if (arrived == n - 1) {
+      atomicExch(cnt, 0u);
       __threadfence();
-      atomicAdd(bar + 1, 1u);
+      atomicAdd(cnt + 1, 1u);
     } else {
       uint32_t it = 0;
       while (*vgen == gen) {
@@ -216,7 +219,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
   __shared__ int s_row_node[kRowsPerTile], s_row_lo[kRowsPerTile];
   __shared__ float s_pmax[2][kRowsPerTile];
   __shared__ float s_m[kRowsPerTile], s_l[2][kRowsPerTile];
-  __shared__ int s_ok, s_C;
+  __shared__ int s_ok;
   __shared__ int s_wpar[kMaxNodes], s_wtok[kMaxNodes];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -267,85 +270,88 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
                         (static_cast<size_t>(node) * p.vocab + begin) * esz,
                bytes, bar);
   };
-  // the logits slice of this CTA (unit blk): 16-byte vectors loaded into
-  // registers at the start and scanned later (attention CTAs scan while
-  // their first MMA runs); slices beyond one per CTA use plain loads
+  // the logits slice of this CTA (unit blk) lands in sQ by TMA at t = 0 and
+  // is scanned from shared memory as soon as it has landed (before Q, which
+  // waits in sV, is converted into sQ); further slices use plain loads
   const bool lhas = p.do_accept && blk < p.lunits;
   const bool lreg = lhas && p.lbulk;
-  uint4 lg[kLogitVecs];
   int lbegin = 0, lnvec = 0;
   if (lreg) {
-    const int node = blk / p.lchunks, ch = blk % p.lchunks;
+    const int ch = blk % p.lchunks;
     lbegin = ch * p.lchunk_len;
     const int lend = min(p.vocab, lbegin + p.lchunk_len);
     lnvec = lend > lbegin ? (lend - lbegin) * esz / 16 : 0;
-    const uint4* vp = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.logits) +
-                                                     (static_cast<size_t>(node) * p.vocab + lbegin) * esz);
-#pragma unroll
-    for (int u = 0; u < kLogitVecs; ++u) {
-      const int v = tid + u * kStepThreads;
-      lg[u] = v < lnvec ? __ldcs(vp + v) : make_uint4(0, 0, 0, 0);
-    }
   }
   auto scan_logits = [&]() {
+    const bool ok = cta_wait(bar_lg, 0, &s_ok, p.status);
     // the thread's maximum over independent chains, then the lowest index
     // holding it (min over independent chains); (max, lowest index) pairs
     // then merge across the CTA
+    const uint4* sv = reinterpret_cast<const uint4*>(sQ);
     float best = -INFINITY;
-    if (esz == 2) {
-      __nv_bfloat162 m2[4];
+    int bidx = INT_MAX;
+    if (ok) {
+      if (esz == 2) {
+        __nv_bfloat162 m2[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) m2[e] = __floats2bfloat162_rn(-INFINITY, -INFINITY);
-#pragma unroll
-      for (int u = 0; u < kLogitVecs; ++u) {
-        if (tid + u * kStepThreads < lnvec) {
-          const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&lg[u]);
+        for (int e = 0; e < 4; ++e) m2[e] = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+#pragma unroll 4
+        for (int v = tid; v < lnvec; v += kStepThreads) {
+          const uint4 x = sv[v];
+          const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&x);
 #pragma unroll
           for (int e = 0; e < 4; ++e) m2[e] = __hmax2(m2[e], b[e]);
         }
-      }
 #pragma unroll
-      for (int e = 0; e < 4; ++e) best = fmaxf(best, fmaxf(__low2float(m2[e]), __high2float(m2[e])));
-    } else {
-      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int u = 0; u < kLogitVecs; ++u) {
-        if (tid + u * kStepThreads < lnvec) {
-          const float* f = reinterpret_cast<const float*>(&lg[u]);
+        for (int e = 0; e < 4; ++e) best = fmaxf(best, fmaxf(__low2float(m2[e]), __high2float(m2[e])));
+      } else {
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 4
+        for (int v = tid; v < lnvec; v += kStepThreads) {
+          const uint4 x = sv[v];
+          const float* f = reinterpret_cast<const float*>(&x);
 #pragma unroll
           for (int e = 0; e < 4; ++e) m4[e] = fmaxf(m4[e], f[e]);
         }
+        best = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       }
-      best = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-    }
-    int i4[4] = {INT_MAX, INT_MAX, INT_MAX, INT_MAX};
-#pragma unroll
-    for (int u = 0; u < kLogitVecs; ++u) {
-      const int v = tid + u * kStepThreads;
-      if (v < lnvec) {
+      int i4[4] = {INT_MAX, INT_MAX, INT_MAX, INT_MAX};
+#pragma unroll 4
+      for (int v = tid; v < lnvec; v += kStepThreads) {
+        const uint4 x = sv[v];
         if (esz == 2) {
-          const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&lg[u]);
+          const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&x);
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             if (__bfloat162float(b[e]) == best) i4[e & 3] = min(i4[e & 3], lbegin + v * 8 + e);
         } else {
-          const float* f = reinterpret_cast<const float*>(&lg[u]);
+          const float* f = reinterpret_cast<const float*>(&x);
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             if (f[e] == best) i4[e] = min(i4[e], lbegin + v * 4 + e);
         }
       }
+      bidx = min(min(i4[0], i4[1]), min(i4[2], i4[3]));
+      if (bidx == INT_MAX) best = -INFINITY;   // no element: loses every merge
     }
-    int bidx = min(min(i4[0], i4[1]), min(i4[2], i4[3]));
-    if (bidx == INT_MAX) best = -INFINITY;   // no element: loses every merge
     block_argmax(best, bidx);
     if (tid == 0) {
       p.arg_part[blk].v = best;
       p.arg_part[blk].idx = bidx;
     }
-    __syncthreads();
+    __syncthreads();   // sQ is free again
   };
   bool lscanned = !lreg;
+  bool signalled = false;
+  // every CTA except the walker: "ctx read, argmax partial written"
+  auto signal_done = [&]() {
+    if (signalled) return;
+    signalled = true;
+    if (p.do_accept && blk != p.walker && tid == 0) {
+      __threadfence();
+      atomicAdd(p.bar + 2, 1u);
+    }
+  };
 
   // ================================================================ phase A
   if (tid == 0) {
@@ -355,6 +361,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
     mbar_init(bar_q, 1);
     mbar_init(bar_lg1, 1);
     fence_mbar_init();
+    if (lreg) issue_logits(blk, sQ, bar_lg);
     if (unit >= 0) {
       // bf16 Q rows of the tile -> sV (row-major staging), one copy per
       // node run of consecutive query heads
@@ -469,6 +476,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
       }
       __syncthreads();
     }
+    if (unit < 0) signal_done();   // (extra slices above are done too)
     // ---- the walker keeps the tree's parents and tokens in smem
     if (blk == p.walker && tid < N) {
       s_wpar[tid] = p.parent[tid];
@@ -525,6 +533,11 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
         s_row_lo[tid] = 0x7fffffff;
       }
     }
+    if (!lscanned) {            // the logits slice (in sQ) first
+      scan_logits();
+      lscanned = true;
+    }
+    signal_done();
     // ---- Q: staged bf16 rows (sV) -> fp16 swizzled (sQ)
     const bool q_ok = cta_wait(bar_q, 0, &s_ok, p.status);
     if (q_ok) {
@@ -664,10 +677,6 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
         }
         tc::commit(bar_mma);
       }
-      if (!lscanned) {          // the logits slice, while the MMA runs
-        scan_logits();
-        lscanned = true;
-      }
       if (!cta_wait(bar_mma, ph_mma, &s_ok, p.status)) { alive = false; break; }
       ph_mma ^= 1u;
       tc::fence_after_sync();
@@ -771,10 +780,6 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
       tc::fence_after_sync();
     }
 
-    if (!lscanned) {
-      scan_logits();
-      lscanned = true;
-    }
     // ---- epilogue: O rows from TMEM -> workspace (or the output when
     // there is one split); 32 x 32 blocks go through smem (sQ is free) so
     // that global stores are row-contiguous
@@ -850,77 +855,24 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
   }
-  if (tid == 0) s_C = C;
-
-  // ================================================================ barrier
-  if (!grid_barrier(p.bar, static_cast<unsigned int>(G), p.status)) return;
-
-  // ---- merge the key splits of a slice of the output rows (CTA 0 is kept
-  // free for the walk when the step has one)
-  if (p.splits > 1) {
-    // CTA index among the merging CTAs (all but the walker)
-    const bool skip = p.do_accept && G > 1 && blk == p.walker;
-    const int nb = (p.do_accept && G > 1) ? G - 1 : G;
-    const int mb = (p.do_accept && G > 1 && blk > p.walker) ? blk - 1 : blk;
-    const int total = p.hkv * p.rows;
-    if (!skip) {
-      const int r0 = static_cast<int>(static_cast<long>(mb) * total / nb);
-      const int r1 = static_cast<int>(static_cast<long>(mb + 1) * total / nb);
-      for (int it = tid; it < (r1 - r0) * (D / 4); it += kStepThreads) {
-        const int gr = r0 + it / (D / 4), d = (it % (D / 4)) * 4;
-        const int hh = gr / p.rows, rg = gr % p.rows;
-        const int mtt = rg / kRowsPerTile, rr = rg % kRowsPerTile;
-        const size_t ubase = static_cast<size_t>(hh * p.n_mt + mtt) * p.splits;
-        constexpr int SB = 8;
-        float M = -INFINITY, lsum = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 1
-        for (int s0 = 0; s0 < p.splits; s0 += SB) {
-          float2 ml[SB];
-          uint2 ov[SB];
-#pragma unroll
-          for (int u = 0; u < SB; ++u) {
-            ml[u] = make_float2(-INFINITY, 0.f);
-            ov[u] = make_uint2(0u, 0u);
-            if (s0 + u < p.splits) {
-              const size_t row = (ubase + s0 + u) * kRowsPerTile + rr;
-              ml[u] = __ldcg(&p.part_ml[row]);
-              ov[u] = __ldcg(reinterpret_cast<const uint2*>(p.part_o + row * D + d));
-            }
-          }
-          float Mb = M;
-#pragma unroll
-          for (int u = 0; u < SB; ++u) Mb = fmaxf(Mb, ml[u].x);
-          if (Mb == -INFINITY) continue;
-          const float a = M == -INFINITY ? 0.f : tc::ex2(M - Mb);
-          lsum *= a;
-          acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
-          M = Mb;
-#pragma unroll
-          for (int u = 0; u < SB; ++u) {
-            if (ml[u].x == -INFINITY) continue;
-            const float w = tc::ex2(ml[u].x - M) * ml[u].y;
-            const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&ov[u].x));
-            const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&ov[u].y));
-            lsum += w;
-            acc.x += w * f01.x;
-            acc.y += w * f01.y;
-            acc.z += w * f23.x;
-            acc.w += w * f23.y;
-          }
-        }
-        const float inv = 1.f / lsum;
-        const int node = rg / p.group, qh = hh * p.group + rg % p.group;
-        *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(node) * p.hq + qh) * D + d) =
-            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-        if (d == 0 && p.lse != nullptr)
-          p.lse[node * p.hq + qh] = (M + log2f(lsum)) * 0.69314718055994531f;
-      }
-    }
-  }
-
-  // ---- the walker: argmax merge, walk, commit
+  // ---- the walker: once every other CTA has read ctx and written its
+  // argmax partial, merge the partials, walk and commit -- all before the
+  // grid barrier, under the attention of the other CTAs
   if (p.do_accept && blk == p.walker) {
+    if (tid == 0) {
+      volatile unsigned int* done = p.bar + 2;
+      uint32_t it = 0;
+      int ok = 1;
+      while (*done < static_cast<unsigned int>(G - 1)) {
+        if (++it > (1u << 24)) { ok = 0; break; }
+        __nanosleep(32);
+      }
+      __threadfence();
+      *done = 0u;                        // ready for the next launch
+      if (!ok) report(p.status, DFV_DEV_TIMEOUT);
+      s_ok = ok;
+    }
+    __syncthreads();
     __shared__ int s_am[kMaxNodes];
     __shared__ int s_path[kMaxNodes];
     __shared__ int s_L;
@@ -991,7 +943,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
       }
     }
     __syncthreads();
-    const int Lc = s_L, Cc = s_C;
+    const int Lc = s_L, Cc = C;
     if (Cc + Lc > p.capacity) {
       if (tid == 0) report(p.status, DFV_DEV_CAPACITY);
     } else {
@@ -1010,6 +962,67 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
       }
       __syncthreads();
       if (tid == 0) *p.ctx_len = Cc + Lc;
+    }
+  }
+
+  // ================================================================ merge
+  // The `splits` CTAs of a (KV head, row tile) group meet at their group's
+  // barrier; each then merges its share of the group's rows over the splits
+  // by log-sum-exp.
+  if (unit >= 0 && p.splits > 1) {
+    const int grp = unit / p.splits, split = unit % p.splits;
+    if (!group_barrier(p.bar + 4 + 2 * grp, static_cast<unsigned int>(p.splits), p.status)) return;
+    const int h_ = grp / p.n_mt, mt_ = grp % p.n_mt;
+    const int rows_t = min(kRowsPerTile, p.rows - mt_ * kRowsPerTile);
+    const int r0 = split * rows_t / p.splits, r1 = (split + 1) * rows_t / p.splits;
+    const size_t ubase = static_cast<size_t>(grp) * p.splits;
+    for (int it = tid; it < (r1 - r0) * (D / 4); it += kStepThreads) {
+      const int rr = r0 + it / (D / 4), d = (it % (D / 4)) * 4;
+      const int rg = mt_ * kRowsPerTile + rr;
+      constexpr int SB = 24;
+      float M = -INFINITY, lsum = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+      for (int s0 = 0; s0 < p.splits; s0 += SB) {
+        float2 ml[SB];
+        uint2 ov[SB];
+#pragma unroll
+        for (int u = 0; u < SB; ++u) {
+          ml[u] = make_float2(-INFINITY, 0.f);
+          ov[u] = make_uint2(0u, 0u);
+          if (s0 + u < p.splits) {
+            const size_t row = (ubase + s0 + u) * kRowsPerTile + rr;
+            ml[u] = __ldcg(&p.part_ml[row]);
+            ov[u] = __ldcg(reinterpret_cast<const uint2*>(p.part_o + row * D + d));
+          }
+        }
+        float Mb = M;
+#pragma unroll
+        for (int u = 0; u < SB; ++u) Mb = fmaxf(Mb, ml[u].x);
+        if (Mb == -INFINITY) continue;
+        const float a = M == -INFINITY ? 0.f : tc::ex2(M - Mb);
+        lsum *= a;
+        acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
+        M = Mb;
+#pragma unroll
+        for (int u = 0; u < SB; ++u) {
+          if (ml[u].x == -INFINITY) continue;
+          const float w = tc::ex2(ml[u].x - M) * ml[u].y;
+          const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&ov[u].x));
+          const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&ov[u].y));
+          lsum += w;
+          acc.x += w * f01.x;
+          acc.y += w * f01.y;
+          acc.z += w * f23.x;
+          acc.w += w * f23.y;
+        }
+      }
+      const float inv = 1.f / lsum;
+      const int node = rg / p.group, qh = h_ * p.group + rg % p.group;
+      *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(node) * p.hq + qh) * D + d) =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+      if (d == 0 && p.lse != nullptr)
+        p.lse[node * p.hq + qh] = (M + log2f(lsum)) * 0.69314718055994531f;
     }
   }
 }
@@ -1048,7 +1061,8 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
     // (kLogitVecs 16-byte vectors per thread), more otherwise
     int lc = sms / n_nodes;
     if (lc < 1) lc = 1;
-    const int per = kLogitVecs * kStepThreads * 16 / esz;
+    const int lim = kLogitVecs * kStepThreads * 16 < tile_b ? kLogitVecs * kStepThreads * 16 : tile_b;
+    const int per = lim / esz;
     const int need = (vocab + per - 1) / per;
     if (lc < need) lc = need;
     const int cap_c = (vocab + 255) / 256;
@@ -1057,8 +1071,7 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
     pl->lunits = n_nodes * lc;
     const int align_el = 16 / esz;
     pl->lchunk_len = (((vocab + lc - 1) / lc) + align_el - 1) / align_el * align_el;
-    pl->lbulk = (static_cast<long>(vocab) * esz % 16 == 0) &&
-                pl->lchunk_len * esz <= kLogitVecs * kStepThreads * 16;
+    pl->lbulk = (static_cast<long>(vocab) * esz % 16 == 0) && pl->lchunk_len * esz <= lim;
   } else {
     pl->lchunks = pl->lunits = pl->lchunk_len = pl->lbulk = 0;
   }
@@ -1076,7 +1089,7 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
   }
   const int rowb = head_dim / 32 * 18;
   pl->ws_bar = 0;
-  pl->ws_arg = 256;
+  pl->ws_arg = a256(static_cast<size_t>(4 + 2 * hkv * pl->n_mt) * sizeof(unsigned int));
   pl->ws_qrows = pl->ws_arg + a256(static_cast<size_t>(pl->lunits) * sizeof(ArgPartial));
   pl->ws_ml = pl->ws_qrows + a256(with_accept ? static_cast<size_t>(n_nodes) * hkv * 2 * rowb : 0);
   const size_t nrow = pl->splits > 1 ? static_cast<size_t>(pl->units) * kRowsPerTile : 0;
