@@ -79,16 +79,18 @@ __device__ __forceinline__ void scan_vec(const uint4& r, int base, float& best, 
   }
 }
 
-// Merge per-thread (best, bidx) over the CTA; result valid in thread 0.
+// Merge per-thread (best, bidx) over a CTA of NT threads; result valid in
+// thread 0.
+template <int NT = kAcceptThreads>
 __device__ __forceinline__ void block_argmax(float& best, int& bidx) {
-  __shared__ float sv[kAcceptThreads / 32];
-  __shared__ int si[kAcceptThreads / 32];
+  __shared__ float sv[NT / 32];
+  __shared__ int si[NT / 32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   warp_argmax(best, bidx);
   if (lane == 0) { sv[warp] = best; si[warp] = bidx; }
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int w = 1; w < kAcceptThreads / 32; ++w)
+    for (int w = 1; w < NT / 32; ++w)
       if (beats(sv[w], si[w], best, bidx)) { best = sv[w]; bidx = si[w]; }
   }
 }
@@ -96,7 +98,7 @@ __device__ __forceinline__ void block_argmax(float& best, int& bidx) {
 // Argmax of one row chunk [begin, end), per thread; elements of each
 // thread are visited in increasing index order. U vectors per thread are in
 // flight at once.
-template <typename T, int U = 4>
+template <typename T, int U = 4, int NT = kAcceptThreads>
 __device__ __forceinline__ void chunk_argmax(const T* row, int begin, int end, float& best,
                                              int& bidx) {
   constexpr int VE = 16 / sizeof(T);
@@ -116,22 +118,22 @@ __device__ __forceinline__ void chunk_argmax(const T* row, int begin, int end, f
   const int vbeg = begin + head;
   const int nvec = (end - vbeg) / VE;
   const uint4* vp = reinterpret_cast<const uint4*>(row + vbeg);
-  for (int v0 = tid; v0 < nvec; v0 += U * kAcceptThreads) {
+  for (int v0 = tid; v0 < nvec; v0 += U * NT) {
     uint4 r[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int v = v0 + u * kAcceptThreads;
+      const int v = v0 + u * NT;
       if (v < nvec) r[u] = __ldcs(vp + v);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int v = v0 + u * kAcceptThreads;
+      const int v = v0 + u * NT;
       if (v < nvec) scan_vec<T>(r[u], vbeg + v * VE, best, bidx);
     }
   }
   // scalar tail
   const int tbeg = vbeg + nvec * VE;
-  for (int k = tbeg + tid; k < end; k += kAcceptThreads) {
+  for (int k = tbeg + tid; k < end; k += NT) {
     const float v = to_f32<T>(row[k]);
     if (v > best || bidx == INT_MAX) { best = v; bidx = k; }
   }

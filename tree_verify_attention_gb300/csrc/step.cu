@@ -43,25 +43,29 @@
 
 namespace dfv {
 
-constexpr int kStepThreads = 256;
+constexpr int kStepThreads = 512;   // 16 warps; four per TMEM lane quadrant
 constexpr int kRowsPerTile = 128;   // UMMA M
 constexpr int kChunk = 128;         // keys per chunk (UMMA N of S, K of P V)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxStepSplits = 256;
+constexpr int kMaxStepGrid = 256;   // CTAs of one launch at most
+constexpr int kMaxStagedSlices = 8; // logits slices one CTA stages at most
+constexpr long kSliceCostBytes = 8192;   // per-slice scan overhead, in bytes of streaming
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kLogitVecs = 16;      // 16-byte logits vectors a thread keeps in flight
 
 struct StepPlan {
-  int rows, n_mt, splits, units, grid, lunits, lchunks, lchunk_len, lbulk, smem;
-  int walker, walker_local, lbase, lcount;
+  int rows, n_mt, splits, units, grid, lunits, lchunks, lchunk_len, lbulk, lstride, smem;
+  int walker, walker_local;
+  uint32_t lslot[kMaxStepGrid];   // per CTA: first logits slice | count << 16
   size_t ws_bar, ws_arg, ws_qrows, ws_ml, ws_o, ws_total;
 };
 
 struct StepParams {
   int n_nodes, max_depth, hq, hkv, group, window, capacity, vocab, logits_dtype;
   int rows, n_mt, splits, units, lunits, lchunks, lchunk_len, lbulk;
+  int lstride;       // bytes between staged slices
   int do_accept;
-  int lbase, lcount;  // CTAs [lbase, lbase + lcount) stream the logits
   int walker;        // CTA that merges the argmax partials, walks and commits
   int walker_local;  // 1: it quantises the tree rows into its own smem
   float scale_log2;
@@ -88,6 +92,7 @@ struct StepParams {
   float2* part_ml;          // [units][128]  (running max, log2 units; sum)
   __half* part_o;           // [units][128][D]  O / sum
   uint32_t* status;
+  uint32_t lslot[kMaxStepGrid];   // per CTA: first staged logits slice | count << 16
 };
 
 // Dynamic shared memory map (bytes from a 1024-aligned base).
@@ -102,6 +107,11 @@ struct StepSmem {
   static constexpr int kV = kK + kKBytes;  // V^ ; bf16 Q rows land here first
   static constexpr int kRawK = kV + kTileB;
   static constexpr int kBars = kRawK + (kBulk ? kChunk * kRowB : 0);
+  // logits staging: an attention unit from past the raw V rows in sK to the
+  // end of sV, a CTA without a unit from sQ to the end of sV
+  static constexpr int kUnitStage = kK + (kBulk ? kChunk * kRowB : 0);
+  static constexpr int kUnitStageBytes = kRawK - kUnitStage;
+  static constexpr int kSpareStageBytes = kRawK;
   static constexpr int kBytes = kBars + 64 + 1024;   // + alignment slack
 };
 
@@ -138,29 +148,35 @@ __device__ __forceinline__ void q4_0_block_chunks(const uint16_t* w, uint4* out)
   }
 }
 
-// Bounded barrier among the `n` CTAs of one group (all co-resident in a
-// cooperative launch); false on timeout.
-__device__ bool group_barrier(unsigned int* cnt, unsigned int n, uint32_t* status) {
+// Bounded barrier among the `n` (< 2^16) CTAs of one group, all co-resident
+// in a cooperative launch; false on timeout. One word holds the arrivals
+// (low 16 bits) and a generation (high 16 bits): each CTA adds 1; the last
+// to arrive adds 2^16 - n, which clears the count and advances the
+// generation in one atomic, so the word needs no reset between launches and
+// a waiter needs one atomic and its polls.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const unsigned int* a) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+  return v;
+}
+
+__device__ bool group_barrier(unsigned int* word, unsigned int n, uint32_t* status) {
   __shared__ int s_gok;
   __syncthreads();
   if (threadIdx.x == 0) {
-    volatile unsigned int* vgen = cnt + 1;
-    const unsigned int gen = *vgen;
-    __threadfence();
-    const unsigned int arrived = atomicAdd(cnt, 1u);
+    __threadfence();   // the CTA's writes before the arrival
+    const unsigned int old = atomicAdd(word, 1u);
     int ok = 1;
-    if (arrived == n - 1) {
-      atomicExch(cnt, 0u);
-      __threadfence();
-      atomicAdd(cnt + 1, 1u);
+    if ((old & 0xFFFFu) == n - 1) {
+      atomicAdd(word, 0x10000u - n);
     } else {
+      const unsigned int gen = old >> 16;
       uint32_t it = 0;
-      while (*vgen == gen) {
-        if (++it > (1u << 24)) { ok = 0; break; }
-        __nanosleep(32);
+      while ((ld_acquire_gpu(word) >> 16) == gen) {
+        if (++it > (1u << 22)) { ok = 0; break; }
       }
     }
-    __threadfence();
+    __threadfence();   // the other CTAs' writes after it
     if (!ok) report(status, DFV_DEV_TIMEOUT);
     s_gok = ok;
   }
@@ -210,15 +226,13 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
   uint64_t* bar_kv = reinterpret_cast<uint64_t*>(smem + L::kBars);
   uint64_t* bar_mma = bar_kv + 1;
   uint64_t* bar_lg = bar_kv + 2;
-  uint64_t* bar_q = bar_kv + 3;
-  uint64_t* bar_lg1 = bar_kv + 4;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_kv + 5);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_kv + 3);
 
   __shared__ int s_J[kMaxNodes], s_dep[kMaxNodes];
   __shared__ uint32_t s_anc[kMaxNodes][kMaskWords];
   __shared__ int s_row_node[kRowsPerTile], s_row_lo[kRowsPerTile];
-  __shared__ float s_pmax[2][kRowsPerTile];
-  __shared__ float s_m[kRowsPerTile], s_l[2][kRowsPerTile];
+  __shared__ float s_pmax[4][kRowsPerTile];
+  __shared__ float s_m[kRowsPerTile], s_l[4][kRowsPerTile];
   __shared__ int s_ok;
   __shared__ int s_wpar[kMaxNodes], s_wtok[kMaxNodes];
 
@@ -226,26 +240,35 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
   const int G = gridDim.x, blk = blockIdx.x;
   const int N = p.n_nodes;
 
-  int C = *p.ctx_len;
-  if (C < 0 || C > p.capacity) {
-    if (blk == 0 && tid == 0) report(p.status, DFV_DEV_CTX);
-    C = C < 0 ? 0 : p.capacity;
-  }
-  const int lo_min = p.window > 0 ? max(0, C - p.window + 1) : 0;
-  const int n_cc = (C - lo_min + kChunk - 1) / kChunk;        // committed chunks
-  const int T = n_cc + (N + kChunk - 1) / kChunk;              // + tree chunks
-
   // ---- this CTA's attention unit
   const int unit = blk < p.units ? blk : -1;
-  int h = 0, mt = 0, c0 = 0, c1 = 0;
+  int h = 0, mt = 0, split = 0;
   if (unit >= 0) {
-    const int split = unit % p.splits;
+    split = unit % p.splits;
     mt = (unit / p.splits) % p.n_mt;
     h = unit / (p.splits * p.n_mt);
-    c0 = static_cast<int>(static_cast<long>(split) * T / p.splits);
-    c1 = static_cast<int>(static_cast<long>(split + 1) * T / p.splits);
   }
   const int esz = p.logits_dtype == DFV_DTYPE_BF16 ? 2 : 4;
+  // the context length, read once by thread 0 (with acquire semantics, so
+  // that its report to the walker below cannot overtake it) and shared
+  // through smem after the first barrier
+  __shared__ int s_C;
+  // Chunks [c0, c1) of the unit; the tree chunk (N <= 65 keys: one chunk,
+  // the last, held by the last split) is processed first, then the
+  // committed ones. first_kv: the first chunk processed is committed.
+  int C = 0, lo_min = 0, n_cc = 0, T = 0, c0 = 0, c1 = 0, n_tree = 0;
+  bool first_kv = false;
+  auto derive = [&]() {
+    lo_min = p.window > 0 ? max(0, C - p.window + 1) : 0;
+    n_cc = (C - lo_min + kChunk - 1) / kChunk;                 // committed chunks
+    T = n_cc + 1;                                              // + the tree chunk
+    if (unit >= 0) {
+      c0 = static_cast<int>(static_cast<long>(split) * T / p.splits);
+      c1 = static_cast<int>(static_cast<long>(split + 1) * T / p.splits);
+      n_tree = c1 > n_cc ? 1 : 0;
+      first_kv = n_tree == 0 && c0 < c1;
+    }
+  };
 
   auto issue_kv = [&](int cc) {
     // raw K -> sRawK, raw V -> sK (consumed before K is dequantised)
@@ -258,36 +281,42 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
     bulk_g2s(sRawK, p.k_cache + off, bytes, bar_kv);
     bulk_g2s(sK, p.v_cache + off, bytes, bar_kv);
   };
-  auto issue_logits = [&](int u, uint8_t* buf, uint64_t* bar) {
-    const int node = u / p.lchunks, ch = u % p.lchunks;
-    const int begin = ch * p.lchunk_len;
-    const int end = min(p.vocab, begin + p.lchunk_len);
-    const uint32_t bytes = end > begin ? static_cast<uint32_t>((end - begin) * esz) : 0u;
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar, bytes);
-    if (bytes)
-      bulk_g2s(buf, static_cast<const uint8_t*>(p.logits) +
-                        (static_cast<size_t>(node) * p.vocab + begin) * esz,
-               bytes, bar);
+
+  // The logits slices [ls0, ls0 + lsn) of this CTA land in smem by TMA at
+  // t = 0 (slice k at lstage + k * lstride) and are scanned as soon as they
+  // have landed: an attention unit stages them past its raw V rows in sK and
+  // on into sV (Q goes straight to sQ; K^ and V^ wait for the scan), a CTA
+  // without a unit from sQ on. When the slices cannot be staged, every CTA
+  // takes slices blk, blk + G, ... with plain loads instead.
+  const uint32_t le = p.do_accept && p.lbulk ? p.lslot[blk] : 0u;
+  const int ls0 = static_cast<int>(le & 0xFFFFu), lsn = static_cast<int>(le >> 16);
+  const bool lreg = lsn > 0;
+  uint8_t* lstage = unit >= 0 ? smem + L::kUnitStage : sQ;
+  // A CTA reports to the walker ("ctx read, my writes done") once everything
+  // the walker reads from it is written: its argmax partials, its share of
+  // the quantised tree rows when those go through the workspace. A CTA with
+  // neither reports right after reading ctx.
+  const bool qshare = p.do_accept && !p.walker_local;
+  const bool has_slices = lreg || (p.do_accept && !p.lbulk && blk < p.lunits);
+  const bool late_signal = has_slices || qshare;
+  auto slice_range = [&](int u, int& begin, int& end) {
+    const int ch = u % p.lchunks;
+    begin = ch * p.lchunk_len;
+    end = min(p.vocab, begin + p.lchunk_len);
+    if (end < begin) end = begin;
   };
-  // the logits slice of this CTA (unit blk) lands in sQ by TMA at t = 0 and
-  // is scanned from shared memory as soon as it has landed (before Q, which
-  // waits in sV, is converted into sQ); further slices use plain loads
-  const bool lhas = p.do_accept && blk < p.lunits;
-  const bool lreg = lhas && p.lbulk;
-  int lbegin = 0, lnvec = 0;
-  if (lreg) {
-    const int ch = blk % p.lchunks;
-    lbegin = ch * p.lchunk_len;
-    const int lend = min(p.vocab, lbegin + p.lchunk_len);
-    lnvec = lend > lbegin ? (lend - lbegin) * esz / 16 : 0;
-  }
   auto scan_logits = [&]() {
     const bool ok = cta_wait(bar_lg, 0, &s_ok, p.status);
+#pragma unroll 1
+    for (int k = 0; k < lsn; ++k) {
+    const int u = ls0 + k;
+    int lbegin, lend;
+    slice_range(u, lbegin, lend);
+    const int lnvec = (lend - lbegin) * esz / 16;
     // the thread's maximum over independent chains, then the lowest index
     // holding it (min over independent chains); (max, lowest index) pairs
     // then merge across the CTA
-    const uint4* sv = reinterpret_cast<const uint4*>(sQ);
+    const uint4* sv = reinterpret_cast<const uint4*>(lstage + k * p.lstride);
     float best = -INFINITY;
     int bidx = INT_MAX;
     if (ok) {
@@ -334,19 +363,16 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
       bidx = min(min(i4[0], i4[1]), min(i4[2], i4[3]));
       if (bidx == INT_MAX) best = -INFINITY;   // no element: loses every merge
     }
-    block_argmax(best, bidx);
+    block_argmax<kStepThreads>(best, bidx);
     if (tid == 0) {
-      p.arg_part[blk].v = best;
-      p.arg_part[blk].idx = bidx;
+      p.arg_part[u].v = best;
+      p.arg_part[u].idx = bidx;
     }
-    __syncthreads();   // sQ is free again
+    __syncthreads();   // the staging buffer is free again
+    }
   };
-  bool lscanned = !lreg;
-  bool signalled = false;
-  // every CTA except the walker: "ctx read, argmax partial written"
+  // the late report: after a barrier that follows every write of the CTA
   auto signal_done = [&]() {
-    if (signalled) return;
-    signalled = true;
     if (p.do_accept && blk != p.walker && tid == 0) {
       __threadfence();
       atomicAdd(p.bar + 2, 1u);
@@ -354,49 +380,90 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
   };
 
   // ================================================================ phase A
+  // Thread 0 first: barriers, the logits copies, the read of ctx, the first
+  // K / V copy -- ahead of its own loads below (the barrier-init fence would
+  // wait for them).
   if (tid == 0) {
     mbar_init(bar_kv, 1);
     mbar_init(bar_mma, 1);
     mbar_init(bar_lg, 1);
-    mbar_init(bar_q, 1);
-    mbar_init(bar_lg1, 1);
     fence_mbar_init();
-    if (lreg) issue_logits(blk, sQ, bar_lg);
-    if (unit >= 0) {
-      // bf16 Q rows of the tile -> sV (row-major staging), one copy per
-      // node run of consecutive query heads
-      const int r0 = mt * kRowsPerTile;
-      const int r1 = min(p.rows, r0 + kRowsPerTile);
+    if (lreg) {
       uint32_t total = 0;
-      for (int rg = r0; rg < r1;) {
-        const int j = rg % p.group;
-        const int run = min(p.group - j, r1 - rg);
-        total += static_cast<uint32_t>(run * D * 2);
-        rg += run;
+      for (int k = 0; k < lsn; ++k) {
+        int b0, b1;
+        slice_range(ls0 + k, b0, b1);
+        total += static_cast<uint32_t>((b1 - b0) * esz);
       }
       fence_proxy_async_smem();
-      mbar_arrive_expect_tx(bar_q, total);
-      for (int rg = r0; rg < r1;) {
-        const int node = rg / p.group, j = rg % p.group;
-        const int run = min(p.group - j, r1 - rg);
-        bulk_g2s(sV + (rg - r0) * D * 2,
-                 p.q + (static_cast<size_t>(node) * p.hq + h * p.group + j) * D,
-                 static_cast<uint32_t>(run * D * 2), bar_q);
-        rg += run;
-      }
-      if constexpr (L::kBulk) {
-        if (c0 < c1 && c0 < n_cc) issue_kv(c0);
+      mbar_arrive_expect_tx(bar_lg, total);
+      for (int k = 0; k < lsn; ++k) {
+        const int u = ls0 + k, node = u / p.lchunks;
+        int b0, b1;
+        slice_range(u, b0, b1);
+        if (b1 > b0)
+          bulk_g2s(lstage + k * p.lstride,
+                   static_cast<const uint8_t*>(p.logits) + (static_cast<size_t>(node) * p.vocab + b0) * esz,
+                   static_cast<uint32_t>((b1 - b0) * esz), bar_lg);
       }
     }
+    C = static_cast<int>(ld_acquire_gpu(reinterpret_cast<const unsigned int*>(p.ctx_len)));
+    if (C < 0 || C > p.capacity) {
+      if (blk == 0) report(p.status, DFV_DEV_CTX);
+      C = C < 0 ? 0 : p.capacity;
+    }
+    s_C = C;
+    derive();
+    if constexpr (L::kBulk) {
+      if (first_kv) issue_kv(c0);
+    }
+    // nothing for the walker to wait for but the read of ctx above
+    if (p.do_accept && blk != p.walker && !late_signal) atomicAdd(p.bar + 2, 1u);
   }
-  if (unit >= 0 && warp == 0) {
+  // the last split's tree rows (its first chunk): this thread's first TP
+  // 16-byte pieces, loaded now and converted when the chunk is built
+  constexpr int TP = 4;
+  const bool tree_split = unit >= 0 && split == p.splits - 1;
+  const int nt_all = min(kChunk, N);
+  const int tree_real = 2 * nt_all * (D / 8);     // 16-byte pieces with data
+  uint4 tv[TP];
+#pragma unroll
+  for (int u = 0; u < TP; ++u) {
+    const int it = tid + u * kStepThreads;
+    tv[u] = make_uint4(0u, 0u, 0u, 0u);
+    if (tree_split && it < tree_real) {
+      const int kvi = it / (nt_all * (D / 8));
+      const int key = (it / (D / 8)) % nt_all, c = it % (D / 8);
+      tv[u] = __ldg(reinterpret_cast<const uint4*>(
+          (kvi ? p.tree_v : p.tree_k) + (static_cast<size_t>(key) * p.hkv + h) * D + c * 8));
+    }
+  }
+  // Q: this thread's 16-byte pieces of the tile's bf16 rows, converted into
+  // the fp16 swizzled tile (sQ) once they have landed; rows past the last
+  // are zero
+  constexpr int QU = kRowsPerTile * (D / 8) / kStepThreads;
+  static_assert(QU >= 1, "Q pieces per thread");
+  uint4 qv[QU];
+  if (unit >= 0) {
+#pragma unroll
+    for (int u = 0; u < QU; ++u) {
+      const int it = tid + u * kStepThreads;
+      const int lr = it / (D / 8), c = it % (D / 8);
+      const int rg = mt * kRowsPerTile + lr;
+      qv[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (rg < p.rows)
+        qv[u] = __ldg(reinterpret_cast<const uint4*>(
+            p.q + (static_cast<size_t>(rg / p.group) * p.hq + h * p.group + rg % p.group) * D + c * 8));
+    }
+  }
+  if (unit >= 0 && warp == 2) {
     tc::tmem_alloc(s_tmem, kTmemCols);
     tc::fence_before_sync();
   }
   // ---- tree: depth and ancestor-or-self masks, by pointer jumping in one
   // warp while the copies are in flight; ceil(log2 N) rounds cover every
   // depth (< N)
-  if (unit >= 0 && warp == 0) {
+  if (unit >= 0 && warp == 1) {
 #pragma unroll
     for (int k = 0; k < 3; ++k) {
       const int n = lane + 32 * k;
@@ -447,36 +514,42 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
       __syncwarp();
     }
   }
-  __syncthreads();   // barriers initialised, tree bookkeeping done
+  if (unit >= 0) {
+#pragma unroll
+    for (int u = 0; u < QU; ++u) {
+      const int it = tid + u * kStepThreads;
+      const int lr = it / (D / 8), c = it % (D / 8);
+      *reinterpret_cast<uint4*>(sQ + tc::sw128_offset(lr, c, kRowsPerTile)) = bf16x8_to_f16x8(qv[u]);
+    }
+  }
+  __syncthreads();   // barriers initialised, tree bookkeeping done, ctx known
+  C = s_C;
+  derive();
 
   // ---- logits: CTAs without an attention unit scan their slice now; slices
   // beyond one per CTA (or unaligned rows) go through plain loads
   if (p.do_accept) {
-    if (unit < 0 && lreg) {
-      scan_logits();
-      lscanned = true;
-    }
-    for (int u = lreg ? blk + G : blk; u < p.lunits; u += G) {
+    if (unit < 0 && lreg) scan_logits();
+    for (int u = p.lbulk ? p.lunits : blk; u < p.lunits; u += G) {
       const int node = u / p.lchunks, ch = u % p.lchunks;
       const int begin = ch * p.lchunk_len;
       const int end = min(p.vocab, begin + p.lchunk_len);
       float best = -INFINITY;
       int bidx = INT_MAX;
       if (esz == 2)
-        chunk_argmax<__nv_bfloat16, 16>(
+        chunk_argmax<__nv_bfloat16, 8, kStepThreads>(
             static_cast<const __nv_bfloat16*>(p.logits) + static_cast<size_t>(node) * p.vocab,
             begin, end, best, bidx);
       else
-        chunk_argmax<float, 16>(static_cast<const float*>(p.logits) + static_cast<size_t>(node) * p.vocab,
+        chunk_argmax<float, 8, kStepThreads>(static_cast<const float*>(p.logits) + static_cast<size_t>(node) * p.vocab,
                                 begin, end, best, bidx);
-      block_argmax(best, bidx);
+      block_argmax<kStepThreads>(best, bidx);
       if (tid == 0) {
         p.arg_part[u].v = best;
         p.arg_part[u].idx = bidx;
       }
       __syncthreads();
     }
-    if (unit < 0) signal_done();   // (extra slices above are done too)
     // ---- the walker keeps the tree's parents and tokens in smem
     if (blk == p.walker && tid < N) {
       s_wpar[tid] = p.parent[tid];
@@ -520,6 +593,11 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
     }
   }
 
+  if (unit < 0 && late_signal) {
+    __syncthreads();   // every thread's partials and tree rows written
+    signal_done();
+  }
+
   if (unit >= 0) {
     if (blk == 0 && tid < N && s_dep[tid] > p.max_depth) report(p.status, DFV_DEV_DEPTH);
     if (tid < kRowsPerTile) {
@@ -533,36 +611,9 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
         s_row_lo[tid] = 0x7fffffff;
       }
     }
-    if (!lscanned) {            // the logits slice (in sQ) first
-      scan_logits();
-      lscanned = true;
-    }
-    signal_done();
-    // ---- Q: staged bf16 rows (sV) -> fp16 swizzled (sQ)
-    const bool q_ok = cta_wait(bar_q, 0, &s_ok, p.status);
-    if (q_ok) {
-      constexpr int QU = kRowsPerTile * (D / 8) / kStepThreads;
-      constexpr int QB = QU < 4 ? QU : 4;
-#pragma unroll 1
-      for (int u0 = 0; u0 < QU; u0 += QB) {
-        uint4 qv[QB];
-#pragma unroll
-        for (int u = 0; u < QB; ++u) {
-          const int it = tid + (u0 + u) * kStepThreads;
-          const int lr = it / (D / 8), c = it % (D / 8);
-          qv[u] = mt * kRowsPerTile + lr < p.rows
-                      ? *reinterpret_cast<const uint4*>(sV + lr * D * 2 + c * 16)
-                      : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < QB; ++u) {
-          const int it = tid + (u0 + u) * kStepThreads;
-          const int lr = it / (D / 8), c = it % (D / 8);
-          *reinterpret_cast<uint4*>(sQ + tc::sw128_offset(lr, c, kRowsPerTile)) = bf16x8_to_f16x8(qv[u]);
-        }
-      }
-    }
-    __syncthreads();
+    if (lreg) scan_logits();    // the staged logits slices first
+    else if (late_signal) __syncthreads();   // every thread's tree rows written
+    if (late_signal) signal_done();
     tc::fence_after_sync();
 
     const uint32_t tmem = *s_tmem;
@@ -570,89 +621,102 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
     const uint32_t t_o = tmem + kChunk;     // O: columns [128, 128 + D)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int r = (warp & 3) * 32 + lane;   // this thread's row
-    const int hc = warp >> 2;               // its half of the keys / of O's columns
+    const int hc = warp >> 2;               // its quarter of the keys / of O's columns
     uint32_t ph_kv = 0, ph_mma = 0;
     float m_run = -INFINITY, l_half = 0.f;
-    bool o_valid = false, alive = q_ok;
+    bool o_valid = false, alive = true;
 
 #pragma unroll 1
-    for (int cc = c0; cc < c1 && alive; ++cc) {
+    for (int i = 0; i < c1 - c0 && alive; ++i) {
+      const int cc = i < n_tree ? T - 1 : c0 + (i - n_tree);
       const bool committed = cc < n_cc;
       const int j0 = lo_min + cc * kChunk;
       const int nk = committed ? min(kChunk, C - j0) : 0;
       if (committed) {
         if constexpr (L::kBulk) {
-          if (tid == 0 && cc != c0) issue_kv(cc);
+          if (tid == 0 && !(i == 0 && first_kv)) issue_kv(cc);
           if (!cta_wait(bar_kv, ph_kv, &s_ok, p.status)) { alive = false; break; }
           ph_kv ^= 1u;
         }
-        // V: raw (sK or global) -> sV [keys][D]; then K: raw -> sK [keys][D]
-#pragma unroll 1
-        for (int kvi = 1; kvi >= 0; --kvi) {
-          uint8_t* dst = kvi ? sV : sK;
-          const uint8_t* base;
-          if constexpr (L::kBulk) base = kvi ? sK : sRawK;
-          else base = (kvi ? p.v_cache : p.k_cache) + (static_cast<size_t>(h) * p.capacity + j0) * L::kRowB;
-          // each thread: kChunk * NB / kStepThreads blocks; all words are
-          // loaded first so the loads overlap
-          constexpr int BPT = kChunk * NB / kStepThreads;
-          constexpr int BB = BPT < 2 ? BPT : 2;
-#pragma unroll 1
-          for (int u0 = 0; u0 < BPT; u0 += BB) {
-            uint16_t w[BB][9];
+        // K: raw (sRawK or global) -> sK, V: raw (sK or global) -> sV, both
+        // [keys][D] swizzled, in one pass. A work item is a pair of Q4_0
+        // blocks (36 bytes = 9 words, 64 elements = one swizzle block) of
+        // one key row. Within a warp, lanes 8i..8i+7 take eight consecutive
+        // keys of the same pair: the 16-byte stores of each 8-lane phase
+        // then fall on 8 distinct swizzled granules, and the 9-word loads
+        // (word stride 9 * pairs-per-row between keys, 9 between pairs)
+        // fall on 32 distinct banks. Every raw word is loaded before the
+        // barrier, so V's raw rows in sK are consumed before K overwrites
+        // them.
+        {
+          constexpr int PPK = D / 64;                     // block pairs per key row
+          constexpr int HALF = kChunk * PPK;              // items per operand
+          constexpr int IPT = (2 * HALF + kStepThreads - 1) / kStepThreads;
+          uint32_t w[IPT][9];
 #pragma unroll
-            for (int u = 0; u < BB; ++u) {
-              const int it = tid + (u0 + u) * kStepThreads;
-              const int key = it / NB, b = it % NB;
-              const uint16_t* src = reinterpret_cast<const uint16_t*>(base + key * L::kRowB + b * 18);
+          for (int u = 0; u < IPT; ++u) {
+            const int g = tid + u * kStepThreads;
+            const int kvi = g / HALF, rem = g % HALF;
+            const int l = rem & 31;
+            const int key = (rem >> 5) * (32 / PPK) + (l & 7) + 8 * (l / (8 * PPK));
+            const int pp = (l >> 3) % PPK;
+            const bool live = g < 2 * HALF && key < nk;
+            const uint8_t* base;
+            if constexpr (L::kBulk) base = kvi ? sK : sRawK;
+            else base = (kvi ? p.v_cache : p.k_cache) + (static_cast<size_t>(h) * p.capacity + j0) * L::kRowB;
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(base + (live ? key * L::kRowB + pp * 36 : 0));
 #pragma unroll
-              for (int e = 0; e < 9; ++e) w[u][e] = key < nk ? src[e] : static_cast<uint16_t>(0);
-            }
+            for (int e = 0; e < 9; ++e) w[u][e] = live ? src[e] : 0u;
+          }
+          if constexpr (L::kBulk) __syncthreads();   // raw V (in sK) consumed
 #pragma unroll
-            for (int u = 0; u < BB; ++u) {
-              const int it = tid + (u0 + u) * kStepThreads;
-              const int key = it / NB, b = it % NB;
-              uint4 o4[4];
-              q4_0_block_chunks(w[u], o4);   // an all-zero block dequantises to zeros
+          for (int u = 0; u < IPT; ++u) {
+            const int g = tid + u * kStepThreads;
+            if (g < 2 * HALF) {
+              const int kvi = g / HALF, rem = g % HALF;
+              const int l = rem & 31;
+              const int key = (rem >> 5) * (32 / PPK) + (l & 7) + 8 * (l / (8 * PPK));
+              const int pp = (l >> 3) % PPK;
+              uint16_t hw[18];
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                *reinterpret_cast<uint4*>(dst + tc::sw128_offset(key, b * 4 + e, kChunk)) = o4[e];
+              for (int e = 0; e < 9; ++e) {
+                hw[2 * e] = static_cast<uint16_t>(w[u][e] & 0xFFFFu);
+                hw[2 * e + 1] = static_cast<uint16_t>(w[u][e] >> 16);
+              }
+              uint4 o4[8];
+              q4_0_block_chunks(hw, o4);       // an all-zero block dequantises to zeros
+              q4_0_block_chunks(hw + 9, o4 + 4);
+              uint8_t* dst = kvi ? sV : sK;
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                *reinterpret_cast<uint4*>(dst + tc::sw128_offset(key, pp * 8 + e, kChunk)) = o4[e];
             }
           }
-          __syncthreads();   // raw V (in sK) consumed before K overwrites it
         }
       } else {
         // tree chunk: keys t = 0..N-1 from tree_k / tree_v (bf16 -> fp16);
-        // the other key rows are zero. The loads of a thread are issued
-        // together.
-        const int t0 = (cc - n_cc) * kChunk;
-        const int nt = max(0, min(kChunk, N - t0));             // real keys here
-        const int real = 2 * nt * (D / 8);                      // 16-byte items with data
-        constexpr int TB = 8;
+        // the other key rows are zero. The first TP pieces of each thread
+        // were loaded at entry.
+        const int nt = nt_all;
+        const int real = tree_real;
+#pragma unroll
+        for (int u = 0; u < TP; ++u) {
+          const int it = tid + u * kStepThreads;
+          if (it < real) {
+            const int kvi = it / (nt * (D / 8));
+            const int key = (it / (D / 8)) % nt, c = it % (D / 8);
+            *reinterpret_cast<uint4*>((kvi ? sV : sK) + tc::sw128_offset(key, c, kChunk)) =
+                bf16x8_to_f16x8(tv[u]);
+          }
+        }
 #pragma unroll 1
-        for (int it0 = tid; it0 < real; it0 += TB * kStepThreads) {
-          uint4 v[TB];
-#pragma unroll
-          for (int u = 0; u < TB; ++u) {
-            const int it = it0 + u * kStepThreads;
-            v[u] = make_uint4(0, 0, 0, 0);
-            if (it < real) {
-              const int kvi = it / (nt * (D / 8));
-              const int key = (it / (D / 8)) % nt, c = it % (D / 8);
-              v[u] = *reinterpret_cast<const uint4*>(
-                  (kvi ? p.tree_v : p.tree_k) + (static_cast<size_t>(t0 + key) * p.hkv + h) * D + c * 8);
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < TB; ++u) {
-            const int it = it0 + u * kStepThreads;
-            if (it < real) {
-              const int kvi = it / (nt * (D / 8));
-              const int key = (it / (D / 8)) % nt, c = it % (D / 8);
-              *reinterpret_cast<uint4*>((kvi ? sV : sK) + tc::sw128_offset(key, c, kChunk)) =
-                  bf16x8_to_f16x8(v[u]);
-            }
-          }
+        for (int it = tid + TP * kStepThreads; it < real; it += kStepThreads) {
+          const int kvi = it / (nt * (D / 8));
+          const int key = (it / (D / 8)) % nt, c = it % (D / 8);
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+              (kvi ? p.tree_v : p.tree_k) + (static_cast<size_t>(key) * p.hkv + h) * D + c * 8));
+          *reinterpret_cast<uint4*>((kvi ? sV : sK) + tc::sw128_offset(key, c, kChunk)) =
+              bf16x8_to_f16x8(v);
         }
         const int zero = 2 * (kChunk - nt) * (D / 8);
         for (int it = tid; it < zero; it += kStepThreads) {
@@ -681,12 +745,11 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
       ph_mma ^= 1u;
       tc::fence_after_sync();
 
-      // ---- masked softmax: two threads per row, 64 keys each
+      // ---- masked softmax: four threads per row, 32 keys each
       {
-        const int kb0 = hc * 64;
-        float s[64];
+        const int kb0 = hc * 32;
+        float s[32];
         tc::ld32(t_s + lane_base + kb0, s);
-        tc::ld32(t_s + lane_base + kb0 + 32, s + 32);
         const int node = s_row_node[r], lo = s_row_lo[r];
         float cm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         const float sc = p.scale_log2;
@@ -695,29 +758,25 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
           const int kmin = min(max(lo - j0, 0), kChunk) - kb0;
           const int kmax = (node >= 0 ? nk : 0) - kb0;
 #pragma unroll
-          for (int k = 0; k < 64; ++k) {
+          for (int k = 0; k < 32; ++k) {
             const float x = (k >= kmin && k < kmax) ? s[k] * sc : -INFINITY;
             s[k] = x;
             cm[k & 3] = fmaxf(cm[k & 3], x);
           }
         } else {
-          // tree keys t = 0..N-1 (N <= 65 < 128: one tree chunk)
-          uint32_t mw0 = 0u, mw1 = 0u;
-          if (node >= 0) {
-            mw0 = s_anc[node][hc * 2];
-            mw1 = hc == 0 ? s_anc[node][1] : 0u;
-          }
+          // tree keys t = 0..N-1 (N <= 65 < 128: one tree chunk); this
+          // thread's keys are ancestor-mask word hc
+          const uint32_t w = (node >= 0 && hc < kMaskWords) ? s_anc[node][hc] : 0u;
 #pragma unroll
-          for (int k = 0; k < 64; ++k) {
-            const uint32_t w = k < 32 ? mw0 : mw1;
-            const float x = ((w >> (k & 31)) & 1u) ? s[k] * sc : -INFINITY;
+          for (int k = 0; k < 32; ++k) {
+            const float x = ((w >> k) & 1u) ? s[k] * sc : -INFINITY;
             s[k] = x;
             cm[k & 3] = fmaxf(cm[k & 3], x);
           }
         }
         s_pmax[hc][r] = fmaxf(fmaxf(cm[0], cm[1]), fmaxf(cm[2], cm[3]));
         __syncthreads();
-        const float cmax = fmaxf(s_pmax[0][r], s_pmax[1][r]);
+        const float cmax = fmaxf(fmaxf(s_pmax[0][r], s_pmax[1][r]), fmaxf(s_pmax[2][r], s_pmax[3][r]));
         float alpha = 1.f;
         bool rescale = false;
         if (m_run == -INFINITY) {
@@ -730,7 +789,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
         const float sub = m_run == -INFINITY ? 0.f : m_run;
         float rs4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < 4; ++c) {
           uint32_t w4[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -739,20 +798,23 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
             rs4[e] += p0 + p1;
             w4[e] = pack_half2(p0, p1);
           }
-          *reinterpret_cast<uint4*>(sK + tc::sw128_offset(r, hc * 8 + c, kRowsPerTile)) =
+          *reinterpret_cast<uint4*>(sK + tc::sw128_offset(r, hc * 4 + c, kRowsPerTile)) =
               make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
         l_half = l_half * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
         if (o_valid && __any_sync(0xffffffffu, rescale)) {
-          // this warp's half of the row's O columns
+          // this warp's quarter of the row's O columns
+          constexpr int CW = D / 4 < 32 ? D / 4 : 32;
 #pragma unroll 1
-          for (int c = 0; c < D / 64; ++c) {
-            const uint32_t col = static_cast<uint32_t>(hc * (D / 2) + c * 32);
+          for (int c = 0; c < (D / 4) / CW; ++c) {
+            const uint32_t col = static_cast<uint32_t>(hc * (D / 4) + c * CW);
             float ov[32];
-            tc::ld32(t_o + lane_base + col, ov);
+            if constexpr (CW == 32) tc::ld32(t_o + lane_base + col, ov);
+            else tc::ld16(t_o + lane_base + col, ov);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] *= alpha;
-            tc::st32(t_o + lane_base + col, ov);
+            for (int e = 0; e < CW; ++e) ov[e] *= alpha;
+            if constexpr (CW == 32) tc::st32(t_o + lane_base + col, ov);
+            else tc::st16(t_o + lane_base + col, ov);
           }
         }
       }
@@ -781,58 +843,64 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
     }
 
     // ---- epilogue: O rows from TMEM -> workspace (or the output when
-    // there is one split); 32 x 32 blocks go through smem (sQ is free) so
-    // that global stores are row-contiguous
+    // there is one split)
     s_l[hc][r] = l_half;
     if (hc == 0) s_m[r] = m_run;
     __syncthreads();
     {
-      float* stage = reinterpret_cast<float*>(sQ) + warp * (32 * 36);
-      // 1 / l of the 8 rows this lane stores (rows 4 i + lane / 8)
-      float inv8[8];
+      // Each warp owns 32 rows (its TMEM lane quadrant) and a quarter of the
+      // D columns, moved in CW-column blocks through smem so that global
+      // stores are row-contiguous. The 16 warps' staging areas (at most
+      // 16 x 32 x 36 floats) run from sQ over sK into sV, all free once the
+      // last MMA has completed.
+      constexpr int CW = D / 4 < 32 ? D / 4 : 32;   // columns per block
+      constexpr int LPR = CW / 4;                    // lanes per row (float4 each)
+      constexpr int RPI = 32 / LPR;                  // rows per store instruction
+      constexpr int NI = 32 / RPI;                   // store instructions per block
+      constexpr int SS = CW + 4;                     // staging row stride (floats)
+      static_assert((kStepThreads / 32) * 32 * SS * 4 <= L::kRawK, "staging overruns sV");
+      float* stage = reinterpret_cast<float*>(sQ) + warp * (32 * SS);
+      float inv[NI];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int row = (warp & 3) * 32 + i * 4 + (lane >> 3);
-        const float l = s_l[0][row] + s_l[1][row];
-        inv8[i] = l > 0.f ? __fdividef(1.f, l) : 0.f;
+      for (int i = 0; i < NI; ++i) {
+        const int row = (warp & 3) * 32 + i * RPI + lane / LPR;
+        const float l = (s_l[0][row] + s_l[1][row]) + (s_l[2][row] + s_l[3][row]);
+        inv[i] = l > 0.f ? __fdividef(1.f, l) : 0.f;
       }
 #pragma unroll 1
-      for (int c = 0; c < D / 64; ++c) {
-        const int col = hc * (D / 2) + c * 32;
+      for (int c = 0; c < (D / 4) / CW; ++c) {
+        const int col = hc * (D / 4) + c * CW;
         float ov[32];
-        tc::ld32(t_o + lane_base + col, ov);
+        if constexpr (CW == 32) tc::ld32(t_o + lane_base + col, ov);
+        else tc::ld16(t_o + lane_base + col, ov);
 #pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          *reinterpret_cast<float4*>(stage + lane * 36 + e) = make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
+        for (int e = 0; e < CW; e += 4)
+          *reinterpret_cast<float4*>(stage + lane * SS + e) = make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
         __syncwarp();
-        // all shared loads first, then the global stores (generic pointers
-        // would otherwise serialise the loop)
-        float4 v[8];
+        float4 v[NI];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int rr = i * 4 + (lane >> 3);             // row within the warp's 32
-          v[i] = *reinterpret_cast<const float4*>(stage + rr * 36 + (lane & 7) * 4);
+        for (int i = 0; i < NI; ++i) {
+          const int rr = i * RPI + lane / LPR;            // row within the warp's 32
+          v[i] = *reinterpret_cast<const float4*>(stage + rr * SS + (lane % LPR) * 4);
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int rr = i * 4 + (lane >> 3);
+        for (int i = 0; i < NI; ++i) {
+          const int rr = i * RPI + lane / LPR;
           const int row = (warp & 3) * 32 + rr;
           const int rg = mt * kRowsPerTile + row;
-          if (rg < p.rows && o_valid && alive && inv8[i] > 0.f) {
-            const float inv = inv8[i];
+          if (rg < p.rows && o_valid && alive && inv[i] > 0.f) {
             float4 w = v[i];
-            w.x *= inv; w.y *= inv; w.z *= inv; w.w *= inv;
+            w.x *= inv[i]; w.y *= inv[i]; w.z *= inv[i]; w.w *= inv[i];
+            const int cc4 = col + (lane % LPR) * 4;
             if (p.splits == 1) {
               const int node = rg / p.group, qh = h * p.group + rg % p.group;
-              *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(node) * p.hq + qh) * D + col +
-                                         (lane & 7) * 4) = w;
+              *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(node) * p.hq + qh) * D + cc4) = w;
             } else {
               __half2 h01 = __floats2half2_rn(w.x, w.y), h23 = __floats2half2_rn(w.z, w.w);
               uint2 hv;
               hv.x = *reinterpret_cast<uint32_t*>(&h01);
               hv.y = *reinterpret_cast<uint32_t*>(&h23);
-              *reinterpret_cast<uint2*>(p.part_o + (static_cast<size_t>(unit) * kRowsPerTile + row) * D +
-                                        col + (lane & 7) * 4) = hv;
+              *reinterpret_cast<uint2*>(p.part_o + (static_cast<size_t>(unit) * kRowsPerTile + row) * D + cc4) = hv;
             }
           }
         }
@@ -840,7 +908,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
       }
       const int rg = mt * kRowsPerTile + r;
       if (hc == 0 && rg < p.rows) {
-        const float m = s_m[r], l = s_l[0][r] + s_l[1][r];
+        const float m = s_m[r];
+        const float l = (s_l[0][r] + s_l[1][r]) + (s_l[2][r] + s_l[3][r]);
         const bool ok = o_valid && alive && l > 0.f;
         if (p.splits == 1) {
           const int node = rg / p.group, qh = h * p.group + rg % p.group;
@@ -968,61 +1037,85 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
   // ================================================================ merge
   // The `splits` CTAs of a (KV head, row tile) group meet at their group's
   // barrier; each then merges its share of the group's rows over the splits
-  // by log-sum-exp.
+  // by log-sum-exp. A thread's first fp16 partials are loaded first; the
+  // (m, l) pairs of the CTA's rows go through smem, where one warp per row
+  // turns them into normalised weights.
   if (unit >= 0 && p.splits > 1) {
     const int grp = unit / p.splits, split = unit % p.splits;
     if (!group_barrier(p.bar + 4 + 2 * grp, static_cast<unsigned int>(p.splits), p.status)) return;
     const int h_ = grp / p.n_mt, mt_ = grp % p.n_mt;
     const int rows_t = min(kRowsPerTile, p.rows - mt_ * kRowsPerTile);
     const int r0 = split * rows_t / p.splits, r1 = (split + 1) * rows_t / p.splits;
-    const size_t ubase = static_cast<size_t>(grp) * p.splits;
-    for (int it = tid; it < (r1 - r0) * (D / 4); it += kStepThreads) {
-      const int rr = r0 + it / (D / 4), d = (it % (D / 4)) * 4;
-      const int rg = mt_ * kRowsPerTile + rr;
-      constexpr int SB = 24;
-      float M = -INFINITY, lsum = 0.f;
+    const int nr = r1 - r0, S = p.splits;
+    const size_t ubase = static_cast<size_t>(grp) * S;
+    constexpr int SB = 20;          // partials of one item in flight at once
+    constexpr int DV = D / 4;       // 4-column items per row
+    const int items = nr * DV;
+    auto load_batch = [&](int it, int s0, uint2* ov) {
+      const int rr = r0 + it / DV, d = (it % DV) * 4;
+#pragma unroll
+      for (int u = 0; u < SB; ++u) {
+        ov[u] = make_uint2(0u, 0u);
+        if (it < items && s0 + u < S)
+          ov[u] = __ldcg(reinterpret_cast<const uint2*>(
+              p.part_o + ((ubase + s0 + u) * kRowsPerTile + rr) * D + d));
+      }
+    };
+    uint2 ov[SB];
+    load_batch(tid, 0, ov);
+    float2* s_ml = reinterpret_cast<float2*>(sQ);              // [nr][S]
+    float* s_w = reinterpret_cast<float*>(s_ml + nr * S);      // [nr][S]
+    for (int i = tid; i < nr * S; i += kStepThreads) {
+      const int rr = i / S, sp = i % S;
+      s_ml[i] = __ldcg(&p.part_ml[(ubase + sp) * kRowsPerTile + r0 + rr]);
+    }
+    __syncthreads();
+    for (int rr = warp; rr < nr; rr += kStepThreads / 32) {
+      float M = -INFINITY;
+      for (int sp = lane; sp < S; sp += 32) M = fmaxf(M, s_ml[rr * S + sp].x);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      float lsum = 0.f;
+      for (int sp = lane; sp < S; sp += 32) {
+        const float2 ml = s_ml[rr * S + sp];
+        const float w = ml.x == -INFINITY ? 0.f : tc::ex2(ml.x - M) * ml.y;
+        s_w[rr * S + sp] = w;
+        lsum += w;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      for (int sp = lane; sp < S; sp += 32) s_w[rr * S + sp] *= inv;
+      if (lane == 0 && p.lse != nullptr) {
+        const int rg = mt_ * kRowsPerTile + r0 + rr;
+        const int node = rg / p.group, qh = h_ * p.group + rg % p.group;
+        p.lse[node * p.hq + qh] = (M + log2f(lsum)) * 0.69314718055994531f;
+      }
+    }
+    __syncthreads();
+    for (int it = tid; it < items; it += kStepThreads) {
+      const int rr = it / DV, d = (it % DV) * 4;
+      const float* w = s_w + rr * S;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
-      for (int s0 = 0; s0 < p.splits; s0 += SB) {
-        float2 ml[SB];
-        uint2 ov[SB];
+      for (int s0 = 0; s0 < S; s0 += SB) {
+        if (it != tid || s0 != 0) load_batch(it, s0, ov);
 #pragma unroll
         for (int u = 0; u < SB; ++u) {
-          ml[u] = make_float2(-INFINITY, 0.f);
-          ov[u] = make_uint2(0u, 0u);
-          if (s0 + u < p.splits) {
-            const size_t row = (ubase + s0 + u) * kRowsPerTile + rr;
-            ml[u] = __ldcg(&p.part_ml[row]);
-            ov[u] = __ldcg(reinterpret_cast<const uint2*>(p.part_o + row * D + d));
+          if (s0 + u < S) {
+            const float wt = w[s0 + u];
+            const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&ov[u].x));
+            const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&ov[u].y));
+            acc.x += wt * f01.x;
+            acc.y += wt * f01.y;
+            acc.z += wt * f23.x;
+            acc.w += wt * f23.y;
           }
         }
-        float Mb = M;
-#pragma unroll
-        for (int u = 0; u < SB; ++u) Mb = fmaxf(Mb, ml[u].x);
-        if (Mb == -INFINITY) continue;
-        const float a = M == -INFINITY ? 0.f : tc::ex2(M - Mb);
-        lsum *= a;
-        acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
-        M = Mb;
-#pragma unroll
-        for (int u = 0; u < SB; ++u) {
-          if (ml[u].x == -INFINITY) continue;
-          const float w = tc::ex2(ml[u].x - M) * ml[u].y;
-          const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&ov[u].x));
-          const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&ov[u].y));
-          lsum += w;
-          acc.x += w * f01.x;
-          acc.y += w * f01.y;
-          acc.z += w * f23.x;
-          acc.w += w * f23.y;
-        }
       }
-      const float inv = 1.f / lsum;
+      const int rg = mt_ * kRowsPerTile + r0 + rr;
       const int node = rg / p.group, qh = h_ * p.group + rg % p.group;
-      *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(node) * p.hq + qh) * D + d) =
-          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-      if (d == 0 && p.lse != nullptr)
-        p.lse[node * p.hq + qh] = (M + log2f(lsum)) * 0.69314718055994531f;
+      *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(node) * p.hq + qh) * D + d) = acc;
     }
   }
 }
@@ -1039,12 +1132,12 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
   if (head_dim != 64 && head_dim != 128 && head_dim != 256) return false;
   if (with_accept && vocab < 1) return false;
   const int sms = sm_count();
-  pl->grid = sms;
+  pl->grid = sms < kMaxStepGrid ? sms : kMaxStepGrid;
   pl->rows = n_nodes * (hq / hkv);
   pl->n_mt = (pl->rows + kRowsPerTile - 1) / kRowsPerTile;
   const long kbound = window > 0 ? (window - 1 < cap ? window - 1 : cap) : cap;
   const long tb = (kbound + kChunk - 1) / kChunk + (n_nodes + kChunk - 1) / kChunk;
-  long s = sms / (hkv * pl->n_mt);
+  long s = pl->grid / (hkv * pl->n_mt);
   if (s > tb) s = tb;
   if (s > kMaxStepSplits) s = kMaxStepSplits;
   if (s < 1) return false;                      // more (head, tile) pairs than SMs
@@ -1052,31 +1145,126 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
   pl->units = hkv * pl->n_mt * pl->splits;
   const int tile_b = kRowsPerTile * head_dim * 2;        // logits staging bytes
   const int esz = logits_dtype == DFV_DTYPE_BF16 ? 2 : 4;
-  // every CTA streams logits (one SM alone can only keep a few tens of KB
-  // in flight, so the stream needs all of them)
-  pl->lbase = 0;
-  pl->lcount = pl->grid;
-  if (with_accept) {
-    // slices: at most one per CTA when they fit the registers of the CTA
-    // (kLogitVecs 16-byte vectors per thread), more otherwise
-    int lc = sms / n_nodes;
-    if (lc < 1) lc = 1;
-    const int lim = kLogitVecs * kStepThreads * 16 < tile_b ? kLogitVecs * kStepThreads * 16 : tile_b;
-    const int per = lim / esz;
-    const int need = (vocab + per - 1) / per;
-    if (lc < need) lc = need;
-    const int cap_c = (vocab + 255) / 256;
-    if (lc > cap_c) lc = cap_c < need ? need : cap_c;
-    pl->lchunks = lc;
-    pl->lunits = n_nodes * lc;
-    const int align_el = 16 / esz;
-    pl->lchunk_len = (((vocab + lc - 1) / lc) + align_el - 1) / align_el * align_el;
-    pl->lbulk = (static_cast<long>(vocab) * esz % 16 == 0) && pl->lchunk_len * esz <= lim;
-  } else {
-    pl->lchunks = pl->lunits = pl->lchunk_len = pl->lbulk = 0;
-  }
   // the walker: a CTA without an attention unit when there is one
   pl->walker = with_accept ? (pl->grid > pl->units ? pl->grid - 1 : 0) : -1;
+  for (int i = 0; i < kMaxStepGrid; ++i) pl->lslot[i] = 0u;
+  pl->lchunks = pl->lunits = pl->lchunk_len = pl->lbulk = pl->lstride = 0;
+  if (with_accept) {
+    // Staged slices go first to the CTAs without an attention unit (the
+    // walker aside), then to the units of a last row tile of at most 32 rows,
+    // then to the other units, the splits holding the tree chunk (whose rows
+    // come straight from global memory) last. Each
+    // CTA stages as many slices as fit its staging bytes. The plan takes the
+    // fewest slices per node that the shortest such prefix of CTAs can hold,
+    // so that the long attention units stay off the logits when the others
+    // suffice; the last tier used shares its slices evenly.
+    const int cap_c = (vocab + 255) / 256;
+    int spare_b, unit_b;
+    switch (head_dim) {
+      case 64: spare_b = StepSmem<64>::kSpareStageBytes; unit_b = StepSmem<64>::kUnitStageBytes; break;
+      case 128: spare_b = StepSmem<128>::kSpareStageBytes; unit_b = StepSmem<128>::kUnitStageBytes; break;
+      default: spare_b = StepSmem<256>::kSpareStageBytes; unit_b = StepSmem<256>::kUnitStageBytes; break;
+    }
+    int octa[kMaxStepGrid], otier[kMaxStepGrid], no = 0;
+    int tcount[4] = {0, 0, 0, 0};
+    for (int b = pl->units; b < pl->grid; ++b)
+      if (b != pl->walker) { octa[no] = b; otier[no++] = 0; ++tcount[0]; }
+    const int last_rows = pl->rows - (pl->n_mt - 1) * kRowsPerTile;
+    const bool light_tile = pl->n_mt > 1 && last_rows <= 32;
+    auto tier = [&](int u) {
+      const int split = u % pl->splits, mt = (u / pl->splits) % pl->n_mt;
+      if (pl->splits > 1 && split == pl->splits - 1) return 3;
+      if (light_tile && mt == pl->n_mt - 1) return 1;
+      return 2;
+    };
+    for (int t = 1; t <= 3; ++t)
+      for (int u = 0; u < pl->units; ++u)
+        if (tier(u) == t) { octa[no] = u; otier[no++] = t; ++tcount[t]; }
+    const int align_el = 16 / esz;
+    auto per_cta = [](long stage_b, long sb) {
+      const long c = stage_b / sb;
+      return c < kMaxStagedSlices ? c : static_cast<long>(kMaxStagedSlices);
+    };
+    int best_lc = -1, best_t = 4, best_len = 0;
+    long best_load = 0;
+    if (static_cast<long>(vocab) * esz % 16 == 0) {
+      const int max_lc = cap_c < 4096 / n_nodes ? cap_c : 4096 / n_nodes;   // partials staged in sQ
+      // the lowest tier that can hold every slice (for some slice count),
+      // then the slice count that puts the least work (bytes, plus a fixed
+      // cost per slice) on each CTA of that tier (fewer slices on a tie)
+      for (int pass = 0; pass < 2; ++pass) {
+        for (int lc = 1; lc <= max_lc; ++lc) {
+          const int len = (((vocab + lc - 1) / lc) + align_el - 1) / align_el * align_el;
+          const long sb = static_cast<long>(len) * esz;
+          if (sb > unit_b) continue;
+          const long need = static_cast<long>(n_nodes) * lc;
+          long held = 0;
+          for (int t = 0; t < 4; ++t) {
+            const long cap_t = per_cta(t == 0 ? spare_b : unit_b, sb) * tcount[t];
+            if (held + cap_t >= need) {
+              if (pass == 0) {
+                if (t < best_t) best_t = t;
+              } else if (t == best_t) {
+                const long load = (need - held + tcount[t] - 1) / tcount[t] * (sb + kSliceCostBytes);
+                if (best_lc < 0 || load < best_load) {
+                  best_lc = lc;
+                  best_len = len;
+                  best_load = load;
+                }
+              }
+              break;
+            }
+            held += cap_t;
+          }
+        }
+      }
+    }
+    if (best_lc > 0) {
+      const long sb = static_cast<long>(best_len) * esz;
+      pl->lchunks = best_lc;
+      pl->lunits = n_nodes * best_lc;
+      pl->lchunk_len = best_len;
+      pl->lstride = static_cast<int>(sb);
+      pl->lbulk = 1;
+      // tiers before the last fill to capacity; the last shares the rest
+      long before = 0;
+      for (int t = 0; t < best_t; ++t) before += per_cta(t == 0 ? spare_b : unit_b, sb) * tcount[t];
+      if (before > pl->lunits) before = pl->lunits;
+      const long rest = pl->lunits - before;
+      const long per_last = per_cta(best_t == 0 ? spare_b : unit_b, sb);
+      int sl = 0, li = 0;
+      for (int i = 0; i < no && sl < pl->lunits; ++i) {
+        const int t = otier[i];
+        if (t > best_t) break;
+        long c;
+        if (t < best_t) {
+          c = per_cta(t == 0 ? spare_b : unit_b, sb);
+        } else {
+          // even share of `rest` over the tcount[t] CTAs of the last tier
+          c = rest / tcount[t] + (li < rest % tcount[t] ? 1 : 0);
+          ++li;
+        }
+        if (c > per_last && t == best_t) c = per_last;
+        if (c > pl->lunits - sl) c = pl->lunits - sl;
+        if (c > 0) {
+          pl->lslot[octa[i]] = static_cast<uint32_t>(sl) | (static_cast<uint32_t>(c) << 16);
+          sl += static_cast<int>(c);
+        }
+      }
+    }
+    if (!pl->lbulk) {
+      // plain loads: CTA b takes slices b, b + grid, ...
+      const int lim = kLogitVecs * kStepThreads * 16 < tile_b ? kLogitVecs * kStepThreads * 16 : tile_b;
+      const int per_l = lim / esz;
+      const int need_l = (vocab + per_l - 1) / per_l;
+      int lc = pl->grid / n_nodes;
+      if (lc < need_l) lc = need_l;
+      if (lc > cap_c) lc = cap_c < need_l ? need_l : cap_c;
+      pl->lchunks = lc;
+      pl->lunits = n_nodes * lc;
+      pl->lchunk_len = (((vocab + lc - 1) / lc) + align_el - 1) / align_el * align_el;
+    }
+  }
   {
     const long qbytes = static_cast<long>(n_nodes) * hkv * 2 * (head_dim / 32 * 18);
     const long room = static_cast<long>(kChunk) * (head_dim > kChunk ? head_dim : kChunk) * 2;  // sK
@@ -1181,11 +1369,11 @@ dfv_status step_launch(bool with_accept, int n_nodes, int max_depth, int hq, int
   p.lchunks = pl.lchunks;
   p.lchunk_len = pl.lchunk_len;
   p.lbulk = pl.lbulk;
+  p.lstride = pl.lstride;
   p.do_accept = with_accept ? 1 : 0;
   p.walker = pl.walker;
   p.walker_local = pl.walker_local;
-  p.lbase = pl.lbase;
-  p.lcount = pl.lcount;
+  for (int i = 0; i < kMaxStepGrid; ++i) p.lslot[i] = pl.lslot[i];
   const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(head_dim));
   p.scale_log2 = sc * 1.4426950408889634f;
   p.ctx_len = ctx_len;
