@@ -164,3 +164,40 @@ def test_step_ctx131072_sampled():
     pairs = [(0, 0), (cfg.n_nodes - 1, cfg.n_q_heads - 1)]
     pairs += [(int(rng.integers(cfg.n_nodes)), int(rng.integers(cfg.n_q_heads))) for _ in range(6)]
     r.run(s, sample=pairs)
+
+
+def _edge_logits(logits, bf16):
+    """Rows that probe the per-node argmax: ties across the vocabulary (the
+    lowest index wins), an all -inf row (index 0), the maximum only at the last
+    index, and equal signed zeros as the maximum (the lower index wins)."""
+    lg = logits.copy()
+    V = lg.shape[1]
+    if bf16:
+        hi, low, ninf, pz, nz = 0x41F0, 0xC0A0, 0xFF80, 0x0000, 0x8000   # 30, -5, -inf, +0, -0
+    else:
+        hi, low, ninf, pz, nz = (np.float32(30.0), np.float32(-5.0), np.float32(-np.inf),
+                                 np.float32(0.0), np.float32(-0.0))
+    lg[0, :] = low
+    lg[0, [V // 3, V // 2, V - 1]] = hi
+    lg[1, :] = ninf
+    lg[2, :] = low
+    lg[2, V - 1] = hi
+    lg[3, :] = low
+    lg[3, ::7] = hi                                         # ties in every slice
+    lg[4, :] = low
+    lg[4, [V // 5, V // 7]] = [nz, pz]                      # -0 after +0 ... lowest index is V // 7
+    lg[5, :] = low
+    lg[5, [V // 9, V // 4]] = [nz, pz]                      # -0 first
+    return lg
+
+
+@pytest.mark.parametrize("cfg", [W.SHORT, W.TINY], ids=lambda c: c.name)
+def test_step_argmax_edges(cfg):
+    r = Run(cfg, cfg.ctx_len + 128, check_fill=False)
+    s = W.make_step(cfg, 7)
+    s = replace(s, logits=_edge_logits(s.logits, s.logits.dtype == np.uint16))
+    r.run(s)
+    am = r.step.argmax.cpu().numpy()
+    V = cfg.vocab
+    assert am[0] == V // 3 and am[1] == 0 and am[2] == V - 1 and am[3] == 0
+    assert am[4] == V // 7 and am[5] == V // 9

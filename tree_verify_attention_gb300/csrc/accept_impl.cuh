@@ -79,8 +79,8 @@ __device__ __forceinline__ void scan_vec(const uint4& r, int base, float& best, 
   }
 }
 
-// Merge per-thread (best, bidx) over a CTA of NT threads; result valid in
-// thread 0.
+// Merge per-thread (best, bidx) over a CTA of NT (<= 1024) threads; result
+// valid in thread 0.
 template <int NT = kAcceptThreads>
 __device__ __forceinline__ void block_argmax(float& best, int& bidx) {
   __shared__ float sv[NT / 32];
@@ -89,9 +89,11 @@ __device__ __forceinline__ void block_argmax(float& best, int& bidx) {
   warp_argmax(best, bidx);
   if (lane == 0) { sv[warp] = best; si[warp] = bidx; }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int w = 1; w < NT / 32; ++w)
-      if (beats(sv[w], si[w], best, bidx)) { best = sv[w]; bidx = si[w]; }
+  if (warp == 0) {
+    // the per-warp results merge in warp 0
+    best = lane < NT / 32 ? sv[lane] : -INFINITY;
+    bidx = lane < NT / 32 ? si[lane] : INT_MAX;
+    warp_argmax(best, bidx);
   }
 }
 

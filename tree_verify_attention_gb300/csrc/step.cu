@@ -65,6 +65,7 @@ struct StepParams {
   int n_nodes, max_depth, hq, hkv, group, window, capacity, vocab, logits_dtype;
   int rows, n_mt, splits, units, lunits, lchunks, lchunk_len, lbulk;
   int lstride;       // bytes between staged slices
+  uint32_t group_m;  // ceil(2^32 / group) (0 when group == 1): row -> node by multiply-high
   int do_accept;
   int walker;        // CTA that merges the argmax partials, walks and commits
   int walker_local;  // 1: it quantises the tree rows into its own smem
@@ -85,8 +86,9 @@ struct StepParams {
   int32_t* path;
   int32_t* out_tokens;
   unsigned int* bar;        // [2] CTAs done with ctx and their argmax partial
-                            // (the walker resets it); [4 + 2 g], [5 + 2 g]:
-                            // arrivals / generation of split group g
+                            // (the walker resets it); [4 + 2 g]: arrivals
+                            // (low 16 bits) and generation of split group g
+  unsigned int* ready;      // [units] generation + 1 once the unit's partial is written
   ArgPartial* arg_part;     // [lunits]
   uint8_t* qrows;           // [N][Hkv][2][row bytes]
   float2* part_ml;          // [units][128]  (running max, log2 units; sum)
@@ -129,59 +131,82 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
   return o;
 }
 
-// One Q4_0 block (2-byte aligned) -> 32 fp16 values in four 16-byte chunks:
-// chunk 0 = values 0..7, 1 = 8..15 (low nibbles), 2 = 16..23, 3 = 24..31.
-__device__ __forceinline__ void q4_0_block_chunks(const uint16_t* w, uint4* out) {
-  const __half dh = __ushort_as_half(w[0]);
+// One Q4_0 block -> 32 fp16 values in four 16-byte chunks (chunk 0 =
+// values 0..7, 1 = 8..15: the low nibbles of code bytes 0..15; 2 = 16..23,
+// 3 = 24..31: their high nibbles). `code` holds the 16 code bytes as four
+// little-endian words, `dbits` the fp16 scale. Each code word becomes four
+// half2 of exact integers 1024 + q (the nibble under the exponent of 1024),
+// then (x - 1032) * d rounds once to fp16.
+__device__ __forceinline__ void q4_0_block_chunks(const uint32_t* code, uint32_t dbits, uint4* out) {
+  const __half dh = __ushort_as_half(static_cast<unsigned short>(dbits & 0xFFFFu));
   const __half2 d2 = __halves2half2(dh, dh);
   const __half2 bias = __float2half2_rn(1032.0f);
   uint32_t* o = reinterpret_cast<uint32_t*>(out);
+  auto scale = [&](uint32_t x) {
+    const __half2 v = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&x), bias), d2);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  };
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const uint32_t u = w[1 + k];
-    const uint32_t lo = 0x64006400u | (u & 0x000Fu) | ((u & 0x0F00u) << 8);
-    const uint32_t hi = 0x64006400u | ((u >> 4) & 0x000Fu) | ((u & 0xF000u) << 4);
-    const __half2 vlo = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&lo), bias), d2);
-    const __half2 vhi = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&hi), bias), d2);
-    o[k] = *reinterpret_cast<const uint32_t*>(&vlo);        // chunks 0,1
-    o[8 + k] = *reinterpret_cast<const uint32_t*>(&vhi);    // chunks 2,3
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t a = __byte_perm(code[k], 0u, 0x4140);   // [b0, 0, b1, 0]
+    const uint32_t b = __byte_perm(code[k], 0u, 0x4342);   // [b2, 0, b3, 0]
+    const int cl = k >> 1, pos = (k & 1) * 2;
+    o[cl * 4 + pos] = scale((a & 0x000F000Fu) | 0x64006400u);                // values 4k, 4k+1
+    o[cl * 4 + pos + 1] = scale((b & 0x000F000Fu) | 0x64006400u);            // 4k+2, 4k+3
+    o[(2 + cl) * 4 + pos] = scale(((a >> 4) & 0x000F000Fu) | 0x64006400u);   // 16+4k, ...
+    o[(2 + cl) * 4 + pos + 1] = scale(((b >> 4) & 0x000F000Fu) | 0x64006400u);
   }
 }
 
-// Bounded barrier among the `n` (< 2^16) CTAs of one group, all co-resident
-// in a cooperative launch; false on timeout. One word holds the arrivals
-// (low 16 bits) and a generation (high 16 bits): each CTA adds 1; the last
-// to arrive adds 2^16 - n, which clears the count and advances the
-// generation in one atomic, so the word needs no reset between launches and
-// a waiter needs one atomic and its polls.
+// Two consecutive Q4_0 blocks (36 bytes as nine little-endian words) -> 64
+// fp16 values in eight 16-byte chunks. The first block's code bytes start
+// two bytes into the words, so they are realigned by funnel shifts.
+__device__ __forceinline__ void q4_0_pair_chunks(const uint32_t* w, uint4* out) {
+  uint32_t ca[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) ca[i] = __funnelshift_r(w[i], w[i + 1], 16);
+  q4_0_block_chunks(ca, w[0], out);
+  q4_0_block_chunks(w + 5, w[4] >> 16, out + 4);
+}
+
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const unsigned int* a) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
   return v;
 }
 
-__device__ bool group_barrier(unsigned int* word, unsigned int n, uint32_t* status) {
-  __shared__ int s_gok;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();   // the CTA's writes before the arrival
-    const unsigned int old = atomicAdd(word, 1u);
-    int ok = 1;
-    if ((old & 0xFFFFu) == n - 1) {
-      atomicAdd(word, 0x10000u - n);
-    } else {
-      const unsigned int gen = old >> 16;
-      uint32_t it = 0;
-      while ((ld_acquire_gpu(word) >> 16) == gen) {
-        if (++it > (1u << 22)) { ok = 0; break; }
-      }
+// Split groups: the `n` (< 2^16) CTAs of a group each add 1 to the group's
+// word at the start of a launch (low 16 bits: arrivals; high 16 bits: a
+// generation); the last to arrive adds 2^16 - n, which clears the count and
+// advances the generation for the next launch. Every CTA reads the same
+// generation g from its own add, and a CTA marks its partial written by
+// storing (g + 1) mod 2^16 to its ready word: values left by earlier launches
+// differ from this launch's, so the words need no reset.
+__device__ __forceinline__ uint32_t group_arrive(unsigned int* word, unsigned int n) {
+  const unsigned int old = atomicAdd(word, 1u);
+  if ((old & 0xFFFFu) == n - 1) atomicAdd(word, 0x10000u - n);
+  return ((old >> 16) + 1u) & 0xFFFFu;
+}
+
+// Waits (bounded) until ready[0..n) all hold `tag`; one warp polls, lane i
+// the words i, i + 32, ...; false on timeout.
+__device__ __forceinline__ bool wait_ready(const unsigned int* ready, int n, uint32_t tag) {
+  const int lane = threadIdx.x & 31;
+  bool ok = true;
+  for (int i = lane; i < n; i += 32) {
+    uint32_t it = 0;
+    while (ld_acquire_gpu(ready + i) != tag) {
+      if (++it > (1u << 22)) { ok = false; break; }
     }
-    __threadfence();   // the other CTAs' writes after it
-    if (!ok) report(status, DFV_DEV_TIMEOUT);
-    s_gok = ok;
+    if (!ok) break;
   }
-  __syncthreads();
-  return s_gok != 0;
+  return __all_sync(0xffffffffu, ok);
+}
+
+// n / d for n < 2^16 and 2 <= d <= 256 as the high word of n * ceil(2^32 / d)
+// (exact in that range); m == 0 stands for d == 1.
+__device__ __forceinline__ int div_small(int n, uint32_t m) {
+  return m == 0u ? n : static_cast<int>(__umulhi(static_cast<uint32_t>(n), m));
 }
 
 // Maximum of a float over the CTA, returned to every thread.
@@ -212,8 +237,254 @@ __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int* s_
 
 // ---------------------------------------------------------------- the kernel
 
+// Argmax partials of this CTA's staged logits slices [ls0, ls0 + lsn) (slice
+// k at lstage + k * lstride), once their copies have landed. One pass per
+// slice: four independent chains per thread, each keeping its running
+// maximum and the first vector that reached it; then the lowest vector
+// holding the thread's maximum is re-read for the lowest element index, and
+// the (max, lowest index) pairs merge across the CTA.
+template <typename LT>
+__device__ __noinline__ void scan_slices(const StepParams& p, const uint8_t* lstage, int ls0, int lsn,
+                                         uint64_t* bar_lg, int* s_ok) {
+  constexpr int esz = static_cast<int>(sizeof(LT));
+  const int tid = threadIdx.x;
+  const bool ok = cta_wait(bar_lg, 0, s_ok, p.status);
+#pragma unroll 1
+  for (int k = 0; k < lsn; ++k) {
+    const int u = ls0 + k;
+    const int lbegin = (u % p.lchunks) * p.lchunk_len;
+    const int lend = max(lbegin, min(p.vocab, lbegin + p.lchunk_len));
+    const int lnvec = (lend - lbegin) * esz / 16;
+    const uint4* sv = reinterpret_cast<const uint4*>(lstage + k * p.lstride);
+    float best = -INFINITY;
+    int bidx = INT_MAX;
+    if (ok) {
+      float bk[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      int vk[4] = {INT_MAX, INT_MAX, INT_MAX, INT_MAX};
+#pragma unroll 1
+      for (int v0 = tid; v0 < lnvec; v0 += 4 * kStepThreads) {
+        uint4 x[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (v0 + c * kStepThreads < lnvec) x[c] = sv[v0 + c * kStepThreads];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (v0 + c * kStepThreads < lnvec) {
+            float mf;
+            if constexpr (esz == 2) {
+              const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&x[c]);
+              const __nv_bfloat162 m = __hmax2(__hmax2(b[0], b[1]), __hmax2(b[2], b[3]));
+              mf = fmaxf(__low2float(m), __high2float(m));
+            } else {
+              const float* f = reinterpret_cast<const float*>(&x[c]);
+              mf = fmaxf(fmaxf(f[0], f[1]), fmaxf(f[2], f[3]));
+            }
+            // the first vector is taken even at -inf (a slice of -inf still
+            // has an argmax: its first element)
+            if (mf > bk[c] || (vk[c] == INT_MAX && mf == mf)) { bk[c] = mf; vk[c] = v0 + c * kStepThreads; }
+          }
+        }
+      }
+      best = fmaxf(fmaxf(bk[0], bk[1]), fmaxf(bk[2], bk[3]));
+      int vm = INT_MAX;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (bk[c] == best && vk[c] < vm) vm = vk[c];
+      if (vm != INT_MAX) {
+        const uint4 x = sv[vm];
+        if constexpr (esz == 2) {
+          const __nv_bfloat16* be = reinterpret_cast<const __nv_bfloat16*>(&x);
+#pragma unroll
+          for (int e = 7; e >= 0; --e)
+            if (__bfloat162float(be[e]) == best) bidx = lbegin + vm * 8 + e;
+        } else {
+          const float* f = reinterpret_cast<const float*>(&x);
+#pragma unroll
+          for (int e = 3; e >= 0; --e)
+            if (f[e] == best) bidx = lbegin + vm * 4 + e;
+        }
+      }
+      if (bidx == INT_MAX) best = -INFINITY;   // no element: loses every merge
+    }
+    block_argmax<kStepThreads>(best, bidx);
+    if (tid == 0) {
+      p.arg_part[u].v = best;
+      p.arg_part[u].idx = bidx;
+    }
+    __syncthreads();   // the staging buffer is free again
+    }
+}
+
+// Argmax partials of logits slices blk, blk + G, ... by plain loads (when the
+// slices cannot be staged in smem).
+template <typename LT>
+__device__ __noinline__ void plain_slices(const StepParams& p, int blk, int G) {
+  for (int u = blk; u < p.lunits; u += G) {
+    const int node = u / p.lchunks, ch = u % p.lchunks;
+    const int begin = ch * p.lchunk_len;
+    const int end = min(p.vocab, begin + p.lchunk_len);
+    float best = -INFINITY;
+    int bidx = INT_MAX;
+    chunk_argmax<LT, 8, kStepThreads>(static_cast<const LT*>(p.logits) + static_cast<size_t>(node) * p.vocab,
+                                      begin, end, best, bidx);
+    block_argmax<kStepThreads>(best, bidx);
+    if (threadIdx.x == 0) {
+      p.arg_part[u].v = best;
+      p.arg_part[u].idx = bidx;
+    }
+    __syncthreads();
+  }
+}
+
+// Q4_0 blocks [b0, b1) of the tree's key / value rows, laid out
+// [node][Hkv][K, V][row bytes] at qdst.
 template <int D>
-__global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
+__device__ __noinline__ void prequant_tree(const StepParams& p, uint8_t* qdst, int b0, int b1) {
+  constexpr int NB = D / 32;
+  constexpr int kRowB = StepSmem<D>::kRowB;
+  for (int it = b0 + static_cast<int>(threadIdx.x); it < b1; it += kStepThreads) {
+    const int b = it % NB;
+    const int kv = (it / NB) & 1;
+    const int hh = (it / (2 * NB)) % p.hkv;
+    const int t = it / (2 * NB * p.hkv);
+    const uint4* v = reinterpret_cast<const uint4*>(
+        (kv ? p.tree_v : p.tree_k) + (static_cast<size_t>(t) * p.hkv + hh) * D + b * 32);
+    uint4 r4[4];
+#pragma unroll
+    for (int u4 = 0; u4 < 4; ++u4) r4[u4] = v[u4];
+    float x[32];
+#pragma unroll
+    for (int u4 = 0; u4 < 4; ++u4) {
+      const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&r4[u4]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(hb[e]);
+        x[u4 * 8 + 2 * e] = f.x;
+        x[u4 * 8 + 2 * e + 1] = f.y;
+      }
+    }
+    q4_0_quantize_block(x, qdst + ((static_cast<size_t>(t) * p.hkv + hh) * 2 + kv) * kRowB + b * 18);
+  }
+}
+
+// The walker: waits until every other CTA has read ctx and written what it
+// owes (argmax partials, tree rows), merges the argmax partials per node,
+// walks the tree from the root and commits the accepted rows to the cache.
+template <int D>
+__device__ __noinline__ void walker_tail(const StepParams& p, int G, int C, uint8_t* sQ, const uint8_t* sK,
+                                         const int* s_wpar, const int* s_wtok) {
+  using L = StepSmem<D>;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int N = p.n_nodes;
+  __shared__ int s_ok;
+  if (tid == 0) {
+    volatile unsigned int* done = p.bar + 2;
+    uint32_t it = 0;
+    int ok = 1;
+    while (*done < static_cast<unsigned int>(G - 1)) {
+      if (++it > (1u << 24)) { ok = 0; break; }
+      __nanosleep(32);
+    }
+    __threadfence();
+    *done = 0u;                        // ready for the next launch
+    if (!ok) report(p.status, DFV_DEV_TIMEOUT);
+    s_ok = ok;
+  }
+  __syncthreads();
+  __shared__ int s_am[kMaxNodes];
+  __shared__ int s_path[kMaxNodes];
+  __shared__ int s_L;
+  // every partial in one round of loads (staged in sQ), then per node
+  ArgPartial* s_ap = reinterpret_cast<ArgPartial*>(sQ);
+  for (int i = tid; i < p.lunits; i += kStepThreads) {
+    ArgPartial a;
+    a.v = __ldcg(&p.arg_part[i].v);
+    a.idx = __ldcg(&p.arg_part[i].idx);
+    s_ap[i] = a;
+  }
+  __syncthreads();
+  for (int node = warp; node < N; node += kStepThreads / 32) {
+    float best = -INFINITY;
+    int bidx = INT_MAX;
+    for (int c = lane; c < p.lchunks; c += 32) {
+      const ArgPartial a = s_ap[node * p.lchunks + c];
+      if (beats(a.v, a.idx, best, bidx)) { best = a.v; bidx = a.idx; }
+    }
+    warp_argmax(best, bidx);
+    if (lane == 0) {
+      s_am[node] = bidx;
+      p.argmax[node] = bidx;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int par[3], tok[3];
+#pragma unroll
+    for (int s = 0; s < 3; ++s) {
+      const int n = lane + 32 * s;
+      par[s] = -2;
+      tok[s] = 0;
+      if (n >= 1 && n < N) {
+        int pa = s_wpar[n];
+        if (pa < 0 || pa >= n) pa = 0;
+        par[s] = pa;
+        tok[s] = s_wtok[n];
+      }
+    }
+    int cur = 0, Lw = 1;
+    if (lane == 0) s_path[0] = 0;
+    for (int itw = 0; itw < N; ++itw) {
+      const int t = s_am[cur];
+      const unsigned b0 = __ballot_sync(0xffffffffu, par[0] == cur && tok[0] == t);
+      const unsigned b1 = __ballot_sync(0xffffffffu, par[1] == cur && tok[1] == t);
+      const unsigned b2 = __ballot_sync(0xffffffffu, par[2] == cur && tok[2] == t);
+      int next = -1;
+      if (b0) next = __ffs(b0) - 1;
+      else if (b1) next = 31 + __ffs(b1);
+      else if (b2) next = 63 + __ffs(b2);
+      if (next < 0) break;
+      if (lane == 0) s_path[Lw] = next;
+      ++Lw;
+      cur = next;
+    }
+    __syncwarp();
+    for (int k = lane; k < N; k += 32) {
+      p.path[k] = k < Lw ? s_path[k] : -1;
+      int ot = -1;
+      if (k < Lw - 1) ot = s_wtok[s_path[k + 1]];
+      else if (k == Lw - 1) ot = s_am[s_path[Lw - 1]];
+      p.out_tokens[k] = ot;
+    }
+    if (lane == 0) {
+      *p.accept_len = Lw;
+      s_L = Lw;
+    }
+  }
+  __syncthreads();
+  const int Lc = s_L, Cc = C;
+  if (Cc + Lc > p.capacity) {
+    if (tid == 0) report(p.status, DFV_DEV_CAPACITY);
+  } else {
+    constexpr int W4 = L::kRowB / 4;
+    const int total = Lc * p.hkv * 2 * W4;
+    for (int it = tid; it < total; it += kStepThreads) {
+      const int w = it % W4;
+      const int kv = (it / W4) & 1;
+      const int hh = (it / (2 * W4)) % p.hkv;
+      const int k = it / (2 * W4 * p.hkv);
+      const size_t so = ((static_cast<size_t>(s_path[k]) * p.hkv + hh) * 2 + kv) * L::kRowB;
+      uint32_t* dst = reinterpret_cast<uint32_t*>(
+          (kv ? p.v_cache : p.k_cache) + (static_cast<size_t>(hh) * p.capacity + Cc + k) * L::kRowB);
+      dst[w] = p.walker_local ? reinterpret_cast<const uint32_t*>(sK + so)[w]
+                              : __ldcg(reinterpret_cast<const uint32_t*>(p.qrows + so) + w);
+    }
+    __syncthreads();
+    if (tid == 0) *p.ctx_len = Cc + Lc;
+  }
+}
+
+template <int D, typename LT>
+__global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_constant__ StepParams p) {
   using L = StepSmem<D>;
   constexpr int NB = D / 32;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -248,11 +519,12 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
     mt = (unit / p.splits) % p.n_mt;
     h = unit / (p.splits * p.n_mt);
   }
-  const int esz = p.logits_dtype == DFV_DTYPE_BF16 ? 2 : 4;
+  constexpr int esz = static_cast<int>(sizeof(LT));   // logits element bytes
   // the context length, read once by thread 0 (with acquire semantics, so
   // that its report to the walker below cannot overtake it) and shared
   // through smem after the first barrier
   __shared__ int s_C;
+  __shared__ uint32_t s_tag;   // this launch's ready tag of the unit's group
   // Chunks [c0, c1) of the unit; the tree chunk (N <= 65 keys: one chunk,
   // the last, held by the last split) is processed first, then the
   // committed ones. first_kv: the first chunk processed is committed.
@@ -263,8 +535,10 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
     n_cc = (C - lo_min + kChunk - 1) / kChunk;                 // committed chunks
     T = n_cc + 1;                                              // + the tree chunk
     if (unit >= 0) {
-      c0 = static_cast<int>(static_cast<long>(split) * T / p.splits);
-      c1 = static_cast<int>(static_cast<long>(split + 1) * T / p.splits);
+      // floor(s * T / splits) without a 64-bit product: T = q * splits + r
+      const int q = T / p.splits, r = T - q * p.splits;
+      c0 = split * q + split * r / p.splits;
+      c1 = (split + 1) * q + (split + 1) * r / p.splits;
       n_tree = c1 > n_cc ? 1 : 0;
       first_kv = n_tree == 0 && c0 < c1;
     }
@@ -304,72 +578,6 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
     begin = ch * p.lchunk_len;
     end = min(p.vocab, begin + p.lchunk_len);
     if (end < begin) end = begin;
-  };
-  auto scan_logits = [&]() {
-    const bool ok = cta_wait(bar_lg, 0, &s_ok, p.status);
-#pragma unroll 1
-    for (int k = 0; k < lsn; ++k) {
-    const int u = ls0 + k;
-    int lbegin, lend;
-    slice_range(u, lbegin, lend);
-    const int lnvec = (lend - lbegin) * esz / 16;
-    // the thread's maximum over independent chains, then the lowest index
-    // holding it (min over independent chains); (max, lowest index) pairs
-    // then merge across the CTA
-    const uint4* sv = reinterpret_cast<const uint4*>(lstage + k * p.lstride);
-    float best = -INFINITY;
-    int bidx = INT_MAX;
-    if (ok) {
-      if (esz == 2) {
-        __nv_bfloat162 m2[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) m2[e] = __floats2bfloat162_rn(-INFINITY, -INFINITY);
-#pragma unroll 4
-        for (int v = tid; v < lnvec; v += kStepThreads) {
-          const uint4 x = sv[v];
-          const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&x);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) m2[e] = __hmax2(m2[e], b[e]);
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) best = fmaxf(best, fmaxf(__low2float(m2[e]), __high2float(m2[e])));
-      } else {
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 4
-        for (int v = tid; v < lnvec; v += kStepThreads) {
-          const uint4 x = sv[v];
-          const float* f = reinterpret_cast<const float*>(&x);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) m4[e] = fmaxf(m4[e], f[e]);
-        }
-        best = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      }
-      int i4[4] = {INT_MAX, INT_MAX, INT_MAX, INT_MAX};
-#pragma unroll 4
-      for (int v = tid; v < lnvec; v += kStepThreads) {
-        const uint4 x = sv[v];
-        if (esz == 2) {
-          const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&x);
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            if (__bfloat162float(b[e]) == best) i4[e & 3] = min(i4[e & 3], lbegin + v * 8 + e);
-        } else {
-          const float* f = reinterpret_cast<const float*>(&x);
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (f[e] == best) i4[e] = min(i4[e], lbegin + v * 4 + e);
-        }
-      }
-      bidx = min(min(i4[0], i4[1]), min(i4[2], i4[3]));
-      if (bidx == INT_MAX) best = -INFINITY;   // no element: loses every merge
-    }
-    block_argmax<kStepThreads>(best, bidx);
-    if (tid == 0) {
-      p.arg_part[u].v = best;
-      p.arg_part[u].idx = bidx;
-    }
-    __syncthreads();   // the staging buffer is free again
-    }
   };
   // the late report: after a barrier that follows every write of the CTA
   auto signal_done = [&]() {
@@ -419,6 +627,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
     }
     // nothing for the walker to wait for but the read of ctx above
     if (p.do_accept && blk != p.walker && !late_signal) atomicAdd(p.bar + 2, 1u);
+    if (unit >= 0 && p.splits > 1)
+      s_tag = group_arrive(p.bar + 4 + 2 * (unit / p.splits), static_cast<unsigned int>(p.splits));
   }
   // the last split's tree rows (its first chunk): this thread's first TP
   // 16-byte pieces, loaded now and converted when the chunk is built
@@ -432,8 +642,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
     const int it = tid + u * kStepThreads;
     tv[u] = make_uint4(0u, 0u, 0u, 0u);
     if (tree_split && it < tree_real) {
-      const int kvi = it / (nt_all * (D / 8));
-      const int key = (it / (D / 8)) % nt_all, c = it % (D / 8);
+      const int ka = it / (D / 8), c = it % (D / 8);
+      const int kvi = ka >= nt_all ? 1 : 0, key = ka - kvi * nt_all;
       tv[u] = __ldg(reinterpret_cast<const uint4*>(
           (kvi ? p.tree_v : p.tree_k) + (static_cast<size_t>(key) * p.hkv + h) * D + c * 8));
     }
@@ -451,9 +661,11 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
       const int lr = it / (D / 8), c = it % (D / 8);
       const int rg = mt * kRowsPerTile + lr;
       qv[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (rg < p.rows)
+      if (rg < p.rows) {
+        const int node = div_small(rg, p.group_m), j = rg - node * p.group;
         qv[u] = __ldg(reinterpret_cast<const uint4*>(
-            p.q + (static_cast<size_t>(rg / p.group) * p.hq + h * p.group + rg % p.group) * D + c * 8));
+            p.q + (static_cast<size_t>(node) * p.hq + h * p.group + j) * D + c * 8));
+      }
     }
   }
   if (unit >= 0 && warp == 2) {
@@ -529,27 +741,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
   // ---- logits: CTAs without an attention unit scan their slice now; slices
   // beyond one per CTA (or unaligned rows) go through plain loads
   if (p.do_accept) {
-    if (unit < 0 && lreg) scan_logits();
-    for (int u = p.lbulk ? p.lunits : blk; u < p.lunits; u += G) {
-      const int node = u / p.lchunks, ch = u % p.lchunks;
-      const int begin = ch * p.lchunk_len;
-      const int end = min(p.vocab, begin + p.lchunk_len);
-      float best = -INFINITY;
-      int bidx = INT_MAX;
-      if (esz == 2)
-        chunk_argmax<__nv_bfloat16, 8, kStepThreads>(
-            static_cast<const __nv_bfloat16*>(p.logits) + static_cast<size_t>(node) * p.vocab,
-            begin, end, best, bidx);
-      else
-        chunk_argmax<float, 8, kStepThreads>(static_cast<const float*>(p.logits) + static_cast<size_t>(node) * p.vocab,
-                                begin, end, best, bidx);
-      block_argmax<kStepThreads>(best, bidx);
-      if (tid == 0) {
-        p.arg_part[u].v = best;
-        p.arg_part[u].idx = bidx;
-      }
-      __syncthreads();
-    }
+    if (unit < 0 && lreg) scan_slices<LT>(p, lstage, ls0, lsn, bar_lg, &s_ok);
+    if (!p.lbulk) plain_slices<LT>(p, blk, G);
     // ---- the walker keeps the tree's parents and tokens in smem
     if (blk == p.walker && tid < N) {
       s_wpar[tid] = p.parent[tid];
@@ -564,32 +757,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
     if (mine) {
       const int nq = p.walker_local ? 1 : G;
       const int bq = p.walker_local ? 0 : blk;
-      const int b0 = static_cast<int>(static_cast<long>(bq) * tot / nq);
-      const int b1 = static_cast<int>(static_cast<long>(bq + 1) * tot / nq);
-      for (int it = b0 + tid; it < b1; it += kStepThreads) {
-        const int b = it % NB;
-        const int kv = (it / NB) & 1;
-        const int hh = (it / (2 * NB)) % p.hkv;
-        const int t = it / (2 * NB * p.hkv);
-        const uint4* v = reinterpret_cast<const uint4*>(
-            (kv ? p.tree_v : p.tree_k) + (static_cast<size_t>(t) * p.hkv + hh) * D + b * 32);
-        uint4 r4[4];
-#pragma unroll
-        for (int u4 = 0; u4 < 4; ++u4) r4[u4] = v[u4];
-        float x[32];
-#pragma unroll
-        for (int u4 = 0; u4 < 4; ++u4) {
-          const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&r4[u4]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = __bfloat1622float2(hb[e]);
-            x[u4 * 8 + 2 * e] = f.x;
-            x[u4 * 8 + 2 * e + 1] = f.y;
-          }
-        }
-        q4_0_quantize_block(x, qdst + ((static_cast<size_t>(t) * p.hkv + hh) * 2 + kv) * L::kRowB +
-                                   b * 18);
-      }
+      prequant_tree<D>(p, qdst, static_cast<int>(static_cast<long>(bq) * tot / nq),
+                       static_cast<int>(static_cast<long>(bq + 1) * tot / nq));
     }
   }
 
@@ -603,7 +772,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
     if (tid < kRowsPerTile) {
       const int rg = mt * kRowsPerTile + tid;
       if (rg < p.rows) {
-        const int node = rg / p.group;
+        const int node = div_small(rg, p.group_m);
         s_row_node[tid] = node;
         s_row_lo[tid] = p.window > 0 ? C + s_dep[node] - p.window + 1 : 0;
       } else {
@@ -611,7 +780,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
         s_row_lo[tid] = 0x7fffffff;
       }
     }
-    if (lreg) scan_logits();    // the staged logits slices first
+    if (lreg) scan_slices<LT>(p, lstage, ls0, lsn, bar_lg, &s_ok);   // the staged logits slices first
     else if (late_signal) __syncthreads();   // every thread's tree rows written
     if (late_signal) signal_done();
     tc::fence_after_sync();
@@ -677,15 +846,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
               const int l = rem & 31;
               const int key = (rem >> 5) * (32 / PPK) + (l & 7) + 8 * (l / (8 * PPK));
               const int pp = (l >> 3) % PPK;
-              uint16_t hw[18];
-#pragma unroll
-              for (int e = 0; e < 9; ++e) {
-                hw[2 * e] = static_cast<uint16_t>(w[u][e] & 0xFFFFu);
-                hw[2 * e + 1] = static_cast<uint16_t>(w[u][e] >> 16);
-              }
               uint4 o4[8];
-              q4_0_block_chunks(hw, o4);       // an all-zero block dequantises to zeros
-              q4_0_block_chunks(hw + 9, o4 + 4);
+              q4_0_pair_chunks(w[u], o4);       // all-zero blocks dequantise to zeros
               uint8_t* dst = kvi ? sV : sK;
 #pragma unroll
               for (int e = 0; e < 8; ++e)
@@ -703,16 +865,16 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
         for (int u = 0; u < TP; ++u) {
           const int it = tid + u * kStepThreads;
           if (it < real) {
-            const int kvi = it / (nt * (D / 8));
-            const int key = (it / (D / 8)) % nt, c = it % (D / 8);
+            const int ka = it / (D / 8), c = it % (D / 8);
+            const int kvi = ka >= nt ? 1 : 0, key = ka - kvi * nt;
             *reinterpret_cast<uint4*>((kvi ? sV : sK) + tc::sw128_offset(key, c, kChunk)) =
                 bf16x8_to_f16x8(tv[u]);
           }
         }
 #pragma unroll 1
         for (int it = tid + TP * kStepThreads; it < real; it += kStepThreads) {
-          const int kvi = it / (nt * (D / 8));
-          const int key = (it / (D / 8)) % nt, c = it % (D / 8);
+          const int ka = it / (D / 8), c = it % (D / 8);
+          const int kvi = ka >= nt ? 1 : 0, key = ka - kvi * nt;
           const uint4 v = __ldg(reinterpret_cast<const uint4*>(
               (kvi ? p.tree_v : p.tree_k) + (static_cast<size_t>(key) * p.hkv + h) * D + c * 8));
           *reinterpret_cast<uint4*>((kvi ? sV : sK) + tc::sw128_offset(key, c, kChunk)) =
@@ -720,8 +882,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
         }
         const int zero = 2 * (kChunk - nt) * (D / 8);
         for (int it = tid; it < zero; it += kStepThreads) {
-          const int kvi = it / ((kChunk - nt) * (D / 8));
-          const int key = nt + (it / (D / 8)) % (kChunk - nt), c = it % (D / 8);
+          const int ka = it / (D / 8), c = it % (D / 8);
+          const int kvi = ka >= kChunk - nt ? 1 : 0, key = nt + ka - kvi * (kChunk - nt);
           *reinterpret_cast<uint4*>((kvi ? sV : sK) + tc::sw128_offset(key, c, kChunk)) =
               make_uint4(0, 0, 0, 0);
         }
@@ -893,7 +1055,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
             w.x *= inv[i]; w.y *= inv[i]; w.z *= inv[i]; w.w *= inv[i];
             const int cc4 = col + (lane % LPR) * 4;
             if (p.splits == 1) {
-              const int node = rg / p.group, qh = h * p.group + rg % p.group;
+              const int node = div_small(rg, p.group_m), qh = h * p.group + rg - node * p.group;
               *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(node) * p.hq + qh) * D + cc4) = w;
             } else {
               __half2 h01 = __floats2half2_rn(w.x, w.y), h23 = __floats2half2_rn(w.z, w.w);
@@ -912,7 +1074,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
         const float l = (s_l[0][r] + s_l[1][r]) + (s_l[2][r] + s_l[3][r]);
         const bool ok = o_valid && alive && l > 0.f;
         if (p.splits == 1) {
-          const int node = rg / p.group, qh = h * p.group + rg % p.group;
+          const int node = div_small(rg, p.group_m), qh = h * p.group + rg - node * p.group;
           if (p.lse != nullptr) p.lse[node * p.hq + qh] = (m + log2f(l)) * 0.69314718055994531f;
         } else {
           p.part_ml[static_cast<size_t>(unit) * kRowsPerTile + r] =
@@ -922,127 +1084,32 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
     }
     tc::fence_before_sync();
     __syncthreads();
+    if (tid == 0 && p.splits > 1) {
+      __threadfence();   // the CTA's partial rows before its ready word
+      asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p.ready + unit), "r"(s_tag) : "memory");
+    }
     if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
   }
   // ---- the walker: once every other CTA has read ctx and written its
   // argmax partial, merge the partials, walk and commit -- all before the
-  // grid barrier, under the attention of the other CTAs
-  if (p.do_accept && blk == p.walker) {
-    if (tid == 0) {
-      volatile unsigned int* done = p.bar + 2;
-      uint32_t it = 0;
-      int ok = 1;
-      while (*done < static_cast<unsigned int>(G - 1)) {
-        if (++it > (1u << 24)) { ok = 0; break; }
-        __nanosleep(32);
-      }
-      __threadfence();
-      *done = 0u;                        // ready for the next launch
-      if (!ok) report(p.status, DFV_DEV_TIMEOUT);
-      s_ok = ok;
-    }
-    __syncthreads();
-    __shared__ int s_am[kMaxNodes];
-    __shared__ int s_path[kMaxNodes];
-    __shared__ int s_L;
-    // every partial in one round of loads (staged in sQ), then per node
-    ArgPartial* s_ap = reinterpret_cast<ArgPartial*>(sQ);
-    for (int i = tid; i < p.lunits; i += kStepThreads) {
-      ArgPartial a;
-      a.v = __ldcg(&p.arg_part[i].v);
-      a.idx = __ldcg(&p.arg_part[i].idx);
-      s_ap[i] = a;
-    }
-    __syncthreads();
-    for (int node = warp; node < N; node += kStepThreads / 32) {
-      float best = -INFINITY;
-      int bidx = INT_MAX;
-      for (int c = lane; c < p.lchunks; c += 32) {
-        const ArgPartial a = s_ap[node * p.lchunks + c];
-        if (beats(a.v, a.idx, best, bidx)) { best = a.v; bidx = a.idx; }
-      }
-      warp_argmax(best, bidx);
-      if (lane == 0) {
-        s_am[node] = bidx;
-        p.argmax[node] = bidx;
-      }
-    }
-    __syncthreads();
-    if (warp == 0) {
-      int par[3], tok[3];
-#pragma unroll
-      for (int s = 0; s < 3; ++s) {
-        const int n = lane + 32 * s;
-        par[s] = -2;
-        tok[s] = 0;
-        if (n >= 1 && n < N) {
-          int pa = s_wpar[n];
-          if (pa < 0 || pa >= n) pa = 0;
-          par[s] = pa;
-          tok[s] = s_wtok[n];
-        }
-      }
-      int cur = 0, Lw = 1;
-      if (lane == 0) s_path[0] = 0;
-      for (int itw = 0; itw < N; ++itw) {
-        const int t = s_am[cur];
-        const unsigned b0 = __ballot_sync(0xffffffffu, par[0] == cur && tok[0] == t);
-        const unsigned b1 = __ballot_sync(0xffffffffu, par[1] == cur && tok[1] == t);
-        const unsigned b2 = __ballot_sync(0xffffffffu, par[2] == cur && tok[2] == t);
-        int next = -1;
-        if (b0) next = __ffs(b0) - 1;
-        else if (b1) next = 31 + __ffs(b1);
-        else if (b2) next = 63 + __ffs(b2);
-        if (next < 0) break;
-        if (lane == 0) s_path[Lw] = next;
-        ++Lw;
-        cur = next;
-      }
-      __syncwarp();
-      for (int k = lane; k < N; k += 32) {
-        p.path[k] = k < Lw ? s_path[k] : -1;
-        int ot = -1;
-        if (k < Lw - 1) ot = s_wtok[s_path[k + 1]];
-        else if (k == Lw - 1) ot = s_am[s_path[Lw - 1]];
-        p.out_tokens[k] = ot;
-      }
-      if (lane == 0) {
-        *p.accept_len = Lw;
-        s_L = Lw;
-      }
-    }
-    __syncthreads();
-    const int Lc = s_L, Cc = C;
-    if (Cc + Lc > p.capacity) {
-      if (tid == 0) report(p.status, DFV_DEV_CAPACITY);
-    } else {
-      constexpr int W4 = L::kRowB / 4;
-      const int total = Lc * p.hkv * 2 * W4;
-      for (int it = tid; it < total; it += kStepThreads) {
-        const int w = it % W4;
-        const int kv = (it / W4) & 1;
-        const int hh = (it / (2 * W4)) % p.hkv;
-        const int k = it / (2 * W4 * p.hkv);
-        const size_t so = ((static_cast<size_t>(s_path[k]) * p.hkv + hh) * 2 + kv) * L::kRowB;
-        uint32_t* dst = reinterpret_cast<uint32_t*>(
-            (kv ? p.v_cache : p.k_cache) + (static_cast<size_t>(hh) * p.capacity + Cc + k) * L::kRowB);
-        dst[w] = p.walker_local ? reinterpret_cast<const uint32_t*>(sK + so)[w]
-                                : __ldcg(reinterpret_cast<const uint32_t*>(p.qrows + so) + w);
-      }
-      __syncthreads();
-      if (tid == 0) *p.ctx_len = Cc + Lc;
-    }
-  }
+  // group barriers, under the attention of the other CTAs
+  if (p.do_accept && blk == p.walker) walker_tail<D>(p, G, C, sQ, sK, s_wpar, s_wtok);
 
   // ================================================================ merge
-  // The `splits` CTAs of a (KV head, row tile) group meet at their group's
-  // barrier; each then merges its share of the group's rows over the splits
-  // by log-sum-exp. A thread's first fp16 partials are loaded first; the
+  // Each of the `splits` CTAs of a (KV head, row tile) group waits for the
+  // group's partials to be marked ready, then merges its share of the
+  // group's rows over the splits by log-sum-exp. A thread's first fp16 partials are loaded first; the
   // (m, l) pairs of the CTA's rows go through smem, where one warp per row
   // turns them into normalised weights.
   if (unit >= 0 && p.splits > 1) {
     const int grp = unit / p.splits, split = unit % p.splits;
-    if (!group_barrier(p.bar + 4 + 2 * grp, static_cast<unsigned int>(p.splits), p.status)) return;
+    if (warp == 0) {
+      const bool ok = wait_ready(p.ready + static_cast<size_t>(grp) * p.splits, p.splits, s_tag);
+      if (!ok && lane == 0) report(p.status, DFV_DEV_TIMEOUT);
+      if (lane == 0) s_ok = ok ? 1 : 0;
+    }
+    __syncthreads();
+    if (!s_ok) return;
     const int h_ = grp / p.n_mt, mt_ = grp % p.n_mt;
     const int rows_t = min(kRowsPerTile, p.rows - mt_ * kRowsPerTile);
     const int r0 = split * rows_t / p.splits, r1 = (split + 1) * rows_t / p.splits;
@@ -1088,7 +1155,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
       for (int sp = lane; sp < S; sp += 32) s_w[rr * S + sp] *= inv;
       if (lane == 0 && p.lse != nullptr) {
         const int rg = mt_ * kRowsPerTile + r0 + rr;
-        const int node = rg / p.group, qh = h_ * p.group + rg % p.group;
+        const int node = div_small(rg, p.group_m), qh = h_ * p.group + rg - node * p.group;
         p.lse[node * p.hq + qh] = (M + log2f(lsum)) * 0.69314718055994531f;
       }
     }
@@ -1114,7 +1181,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(StepParams p) {
         }
       }
       const int rg = mt_ * kRowsPerTile + r0 + rr;
-      const int node = rg / p.group, qh = h_ * p.group + rg % p.group;
+      const int node = div_small(rg, p.group_m), qh = h_ * p.group + rg - node * p.group;
       *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(node) * p.hq + qh) * D + d) = acc;
     }
   }
@@ -1277,7 +1344,7 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
   }
   const int rowb = head_dim / 32 * 18;
   pl->ws_bar = 0;
-  pl->ws_arg = a256(static_cast<size_t>(4 + 2 * hkv * pl->n_mt) * sizeof(unsigned int));
+  pl->ws_arg = a256(static_cast<size_t>(4 + 2 * hkv * pl->n_mt + pl->units) * sizeof(unsigned int));
   pl->ws_qrows = pl->ws_arg + a256(static_cast<size_t>(pl->lunits) * sizeof(ArgPartial));
   pl->ws_ml = pl->ws_qrows + a256(with_accept ? static_cast<size_t>(n_nodes) * hkv * 2 * rowb : 0);
   const size_t nrow = pl->splits > 1 ? static_cast<size_t>(pl->units) * kRowsPerTile : 0;
@@ -1286,17 +1353,17 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
   return true;
 }
 
-template <int D>
-static dfv_status step_launch_d(StepParams& p, const StepPlan& pl, cudaStream_t stream) {
+template <int D, typename LT>
+static dfv_status step_launch_dt(StepParams& p, const StepPlan& pl, cudaStream_t stream) {
   static int configured[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DFV_ERR_CUDA;
   if (!configured[dev]) {
-    if (cudaFuncSetAttribute(step_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(step_kernel<D, LT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              StepSmem<D>::kBytes) != cudaSuccess)
       return DFV_ERR_CUDA;
     int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, step_kernel<D>, kStepThreads,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, step_kernel<D, LT>, kStepThreads,
                                                       StepSmem<D>::kBytes) != cudaSuccess ||
         nb < 1)
       return DFV_ERR_CUDA;
@@ -1312,7 +1379,15 @@ static dfv_status step_launch_d(StepParams& p, const StepPlan& pl, cudaStream_t 
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, step_kernel<D>, p) == cudaSuccess ? DFV_OK : DFV_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, step_kernel<D, LT>, p) == cudaSuccess ? DFV_OK : DFV_ERR_CUDA;
+}
+
+// One instantiation per logits element type (the attention-only launch has
+// no logits and takes the bf16 one).
+template <int D>
+static dfv_status step_launch_d(StepParams& p, const StepPlan& pl, cudaStream_t stream) {
+  if (p.do_accept && p.logits_dtype == DFV_DTYPE_F32) return step_launch_dt<D, float>(p, pl, stream);
+  return step_launch_dt<D, __nv_bfloat16>(p, pl, stream);
 }
 
 // Workspace of either logits element size (the slicing differs slightly).
@@ -1357,6 +1432,7 @@ dfv_status step_launch(bool with_accept, int n_nodes, int max_depth, int hq, int
   p.hq = hq;
   p.hkv = hkv;
   p.group = hq / hkv;
+  p.group_m = p.group == 1 ? 0u : static_cast<uint32_t>(((1ull << 32) + p.group - 1) / p.group);
   p.window = window;
   p.capacity = cap;
   p.vocab = vocab;
@@ -1393,6 +1469,7 @@ dfv_status step_launch(bool with_accept, int n_nodes, int max_depth, int hq, int
   p.out_tokens = out_tokens;
   char* ws = static_cast<char*>(workspace);
   p.bar = reinterpret_cast<unsigned int*>(ws + pl.ws_bar);
+  p.ready = p.bar + 4 + 2 * hkv * pl.n_mt;
   p.arg_part = reinterpret_cast<ArgPartial*>(ws + pl.ws_arg);
   p.qrows = reinterpret_cast<uint8_t*>(ws + pl.ws_qrows);
   p.part_ml = reinterpret_cast<float2*>(ws + pl.ws_ml);
