@@ -175,19 +175,6 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const unsigned int* a) {
   return v;
 }
 
-// Split groups: the `n` (< 2^16) CTAs of a group each add 1 to the group's
-// word at the start of a launch (low 16 bits: arrivals; high 16 bits: a
-// generation); the last to arrive adds 2^16 - n, which clears the count and
-// advances the generation for the next launch. Every CTA reads the same
-// generation g from its own add, and a CTA marks its partial written by
-// storing (g + 1) mod 2^16 to its ready word: values left by earlier launches
-// differ from this launch's, so the words need no reset.
-__device__ __forceinline__ uint32_t group_arrive(unsigned int* word, unsigned int n) {
-  const unsigned int old = atomicAdd(word, 1u);
-  if ((old & 0xFFFFu) == n - 1) atomicAdd(word, 0x10000u - n);
-  return ((old >> 16) + 1u) & 0xFFFFu;
-}
-
 // Waits (bounded) until ready[0..n) all hold `tag`; one warp polls, lane i
 // the words i, i + 32, ...; false on timeout.
 __device__ __forceinline__ bool wait_ready(const unsigned int* ready, int n, uint32_t tag) {
@@ -588,48 +575,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
   };
 
   // ================================================================ phase A
-  // Thread 0 first: barriers, the logits copies, the read of ctx, the first
-  // K / V copy -- ahead of its own loads below (the barrier-init fence would
-  // wait for them).
-  if (tid == 0) {
-    mbar_init(bar_kv, 1);
-    mbar_init(bar_mma, 1);
-    mbar_init(bar_lg, 1);
-    fence_mbar_init();
-    if (lreg) {
-      uint32_t total = 0;
-      for (int k = 0; k < lsn; ++k) {
-        int b0, b1;
-        slice_range(ls0 + k, b0, b1);
-        total += static_cast<uint32_t>((b1 - b0) * esz);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(bar_lg, total);
-      for (int k = 0; k < lsn; ++k) {
-        const int u = ls0 + k, node = u / p.lchunks;
-        int b0, b1;
-        slice_range(u, b0, b1);
-        if (b1 > b0)
-          bulk_g2s(lstage + k * p.lstride,
-                   static_cast<const uint8_t*>(p.logits) + (static_cast<size_t>(node) * p.vocab + b0) * esz,
-                   static_cast<uint32_t>((b1 - b0) * esz), bar_lg);
-      }
-    }
-    C = static_cast<int>(ld_acquire_gpu(reinterpret_cast<const unsigned int*>(p.ctx_len)));
-    if (C < 0 || C > p.capacity) {
-      if (blk == 0) report(p.status, DFV_DEV_CTX);
-      C = C < 0 ? 0 : p.capacity;
-    }
-    s_C = C;
-    derive();
-    if constexpr (L::kBulk) {
-      if (first_kv) issue_kv(c0);
-    }
-    // nothing for the walker to wait for but the read of ctx above
-    if (p.do_accept && blk != p.walker && !late_signal) atomicAdd(p.bar + 2, 1u);
-    if (unit >= 0 && p.splits > 1)
-      s_tag = group_arrive(p.bar + 4 + 2 * (unit / p.splits), static_cast<unsigned int>(p.splits));
-  }
+  unsigned int arrive_old = 0;   // thread 0: its add to the split group's word
   // the last split's tree rows (its first chunk): this thread's first TP
   // 16-byte pieces, loaded now and converted when the chunk is built
   constexpr int TP = 4;
@@ -667,6 +613,49 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
             p.q + (static_cast<size_t>(node) * p.hq + h * p.group + j) * D + c * 8));
       }
     }
+  }
+  // Thread 0 first: barriers, the logits copies, the read of ctx, the first
+  // K / V copy -- ahead of its own loads below (the barrier-init fence would
+  // wait for them).
+  if (tid == 0) {
+    mbar_init(bar_kv, 1);
+    mbar_init(bar_mma, 1);
+    mbar_init(bar_lg, 1);
+    fence_mbar_init();
+    C = static_cast<int>(ld_acquire_gpu(reinterpret_cast<const unsigned int*>(p.ctx_len)));
+    // the group arrival's old value is only needed at the end of the unit
+    if (unit >= 0 && p.splits > 1) arrive_old = atomicAdd(p.bar + 4 + 2 * (unit / p.splits), 1u);
+    if (C < 0 || C > p.capacity) {
+      if (blk == 0) report(p.status, DFV_DEV_CTX);
+      C = C < 0 ? 0 : p.capacity;
+    }
+    s_C = C;
+    derive();
+    if constexpr (L::kBulk) {
+      if (first_kv) issue_kv(c0);
+    }
+    // the logits copies go after the K/V copy, which is on the critical path
+    if (lreg) {
+      uint32_t total = 0;
+      for (int k = 0; k < lsn; ++k) {
+        int b0, b1;
+        slice_range(ls0 + k, b0, b1);
+        total += static_cast<uint32_t>((b1 - b0) * esz);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar_lg, total);
+      for (int k = 0; k < lsn; ++k) {
+        const int u = ls0 + k, node = u / p.lchunks;
+        int b0, b1;
+        slice_range(u, b0, b1);
+        if (b1 > b0)
+          bulk_g2s(lstage + k * p.lstride,
+                   static_cast<const uint8_t*>(p.logits) + (static_cast<size_t>(node) * p.vocab + b0) * esz,
+                   static_cast<uint32_t>((b1 - b0) * esz), bar_lg);
+      }
+    }
+    // nothing for the walker to wait for but the read of ctx above
+    if (p.do_accept && blk != p.walker && !late_signal) atomicAdd(p.bar + 2, 1u);
   }
   if (unit >= 0 && warp == 2) {
     tc::tmem_alloc(s_tmem, kTmemCols);
@@ -1085,6 +1074,14 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     tc::fence_before_sync();
     __syncthreads();
     if (tid == 0 && p.splits > 1) {
+      // The split group's word: each CTA adds 1 (low 16 bits: arrivals;
+      // high 16 bits: a generation); the last to arrive adds 2^16 - n, which
+      // clears the count and advances the generation for the next launch.
+      // Every CTA of the group reads the same generation g from its own add
+      // and marks its partial written with (g + 1) mod 2^16.
+      const unsigned int n = static_cast<unsigned int>(p.splits);
+      if ((arrive_old & 0xFFFFu) == n - 1) atomicAdd(p.bar + 4 + 2 * (unit / p.splits), 0x10000u - n);
+      s_tag = ((arrive_old >> 16) + 1u) & 0xFFFFu;
       __threadfence();   // the CTA's partial rows before its ready word
       asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p.ready + unit), "r"(s_tag) : "memory");
     }
@@ -1104,6 +1101,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
   if (unit >= 0 && p.splits > 1) {
     const int grp = unit / p.splits, split = unit % p.splits;
     if (warp == 0) {
+      __syncwarp();   // s_tag was written by lane 0
       const bool ok = wait_ready(p.ready + static_cast<size_t>(grp) * p.splits, p.splits, s_tag);
       if (!ok && lane == 0) report(p.status, DFV_DEV_TIMEOUT);
       if (lane == 0) s_ok = ok ? 1 : 0;
