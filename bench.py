@@ -218,6 +218,7 @@ class CacheView:
     def __init__(self, k, v, ctx_len, n_kv_heads, head_dim, capacity):
         self.k, self.v, self.ctx_len = k, v, ctx_len
         self.n_kv_heads, self.head_dim, self.capacity = n_kv_heads, head_dim, capacity
+        self.fmt, self.kv_format = "q4_0", 2
 
 
 def algorithmic_per_step(cfg, parents):

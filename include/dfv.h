@@ -40,11 +40,16 @@
  *
  * Data layouts
  * ------------
- * KV cache (K and V each): Q4_0 blocks, [n_kv_heads][cache_capacity][D/32],
- *   one block = 18 bytes: fp16 scale d, then 16 bytes of 4-bit codes (byte j
- *   = code j in the low nibble, code j+16 in the high nibble); the block's
- *   values are (code - 8) * d. Row (head h, position p) starts at byte
- *   (h * cache_capacity + p) * (D / 32) * 18. Base pointer 16-byte aligned.
+ * KV cache (K and V each), kv_format DFV_KV_Q4_0: Q4_0 blocks,
+ *   [n_kv_heads][cache_capacity][D/32], one block = 18 bytes: fp16 scale d,
+ *   then 16 bytes of 4-bit codes (byte j = code j in the low nibble, code
+ *   j+16 in the high nibble); the block's values are (code - 8) * d. Row
+ *   (head h, position p) starts at byte (h * cache_capacity + p) * (D / 32)
+ *   * 18. Base pointer 16-byte aligned.
+ * KV cache, kv_format DFV_KV_F16 ("Luce DFlash ..." results paragraph: the
+ *   F16 cache that Q4_0 is compared against): binary16 values,
+ *   [n_kv_heads][cache_capacity][D], row (h, p) at byte
+ *   (h * cache_capacity + p) * D * 2; written with round-to-nearest-even.
  * Tree nodes: node 0 is the root; parent[i] in [0, i) for i >= 1 (parent[0]
  *   is ignored). Committed key j sits at position j, node i at position
  *   ctx_len + depth(i).
@@ -80,7 +85,13 @@ typedef enum dfv_status {
 #define DFV_DEV_BAD_PATH 0x10u /* path entry outside [0, n_nodes): no write   */
 #define DFV_DEV_TIMEOUT 0x20u  /* a bounded wait gave up; outputs undefined   */
 
-#define DFV_KV_Q4_0 2 /* the only KV format ("Q4_0", 18-byte blocks) */
+#define DFV_KV_F16 1  /* binary16 values, 2 * D bytes per row                */
+#define DFV_KV_Q4_0 2 /* Q4_0 blocks, D / 32 * 18 bytes per row               */
+/* Flag OR-ed into kv_format of the attention entry points: attend the tree
+ * nodes' K/V as the commit stores them in the cache format (Q4_0: quantised
+ * and dequantised; F16: rounded to binary16, exact for bf16 values in
+ * range), instead of their bf16 values. */
+#define DFV_KV_TREE_AS_CACHE 0x100
 
 #define DFV_DTYPE_F32 0
 #define DFV_DTYPE_BF16 1
@@ -94,7 +105,7 @@ const char* dfv_status_string(dfv_status s);
 int dfv_version(void);
 
 /* ------------------------------------------------------------------------
- * dfv_tree_verify_attn -- tree-masked attention over a Q4_0 cache.
+ * dfv_tree_verify_attn -- tree-masked attention over a Q4_0 (or F16) cache.
  *
  * Passage: "Luce DFlash: Qwen3.6-27B ..." (ai-navigate-news, ja), feature
  * list -- DDTree tree-verify (block 16, budget 22) and sliding-window flash
@@ -102,17 +113,20 @@ int dfv_version(void);
  *
  * out[i][h][:] = sum_k softmax_k(scale * q[i][h] . key_k) * value_k over the
  * keys visible to node i (see "Visibility" above); committed keys/values are
- * the cache's Q4_0 rows dequantised, tree keys/values are tree_k / tree_v.
+ * the cache's rows decoded (Q4_0 dequantised, F16 widened), tree keys/values
+ * are tree_k / tree_v (with DFV_KV_TREE_AS_CACHE: those rows as the commit
+ * would store them, decoded -- the reading in which tree rows are written to
+ * the cache before attention and rollback truncates).
  *
  *   n_nodes        N = budget + 1, 1..DFV_MAX_NODES
  *   max_depth      bound on tree depth (block size); deeper -> DFV_DEV_DEPTH
  *   n_q_heads      Hq;  n_kv_heads Hkv; Hq % Hkv == 0, Hq <= 256
  *   head_dim       D in {64, 128, 256}
  *   window         sliding window in positions, 0 = none
- *   kv_format      DFV_KV_Q4_0
+ *   kv_format      DFV_KV_Q4_0 or DFV_KV_F16, optionally | DFV_KV_TREE_AS_CACHE
  *   cache_capacity positions per head in the cache
  *   ctx_len        device int32[1], committed length C (read only)
- *   k_cache,v_cache  device Q4_0 cache (layout above), read only
+ *   k_cache,v_cache  device cache in kv_format (layout above), read only
  *   q              device bf16 [N][Hq][D]
  *   tree_k,tree_v  device bf16 [N][Hkv][D], the tree nodes' own K/V rows
  *   parent         device int32 [N]
@@ -212,8 +226,10 @@ dfv_status dfv_greedy_accept_static(int n_nodes, int vocab, int logits_dtype, co
  * "What we ported and tuned": Q4_0 KV cache; "Luce DFlash ..." feature list:
  * tree-verify over that cache.
  *
- * For k < L = *accept_len and every KV head h, quantises tree_k[path[k]][h]
- * (and tree_v) to Q4_0 and writes it at cache position C + k, C = *ctx_len;
+ * For k < L = *accept_len and every KV head h, encodes tree_k[path[k]][h]
+ * (and tree_v) in kv_format (DFV_KV_Q4_0: the rule below; DFV_KV_F16:
+ * binary16, round-to-nearest-even) and writes it at cache position C + k,
+ * C = *ctx_len;
  * then *ctx_len = C + L. Positions >= C + L are not touched (rejected nodes
  * are never written). If C + L > cache_capacity, or a path entry is outside
  * [0, n_nodes), nothing is written, *ctx_len is unchanged and a DFV_DEV_*
@@ -228,7 +244,7 @@ dfv_status dfv_greedy_accept_static(int n_nodes, int vocab, int logits_dtype, co
  *   ctx_len       device int32[1], read and advanced
  *   accept_len    device int32[1];  path device int32 [>= L]
  *   tree_k/v      device bf16 [N][Hkv][D]
- *   k_cache/v_cache  device Q4_0 cache, written at rows [C, C + L)
+ *   k_cache/v_cache  device cache in kv_format, written at rows [C, C + L)
  * ---------------------------------------------------------------------- */
 dfv_status dfv_kv_commit(int n_nodes, int n_kv_heads, int head_dim, int kv_format,
                          int cache_capacity, int32_t* ctx_len, const int32_t* accept_len,
@@ -237,11 +253,12 @@ dfv_status dfv_kv_commit(int n_nodes, int n_kv_heads, int head_dim, int kv_forma
 
 /* ------------------------------------------------------------------------
  * dfv_kv_quantize_rows -- fill cache rows [pos0, pos0 + n_rows) of every KV
- * head from float rows, with the Q4_0 rule of dfv_kv_commit (prefill).
+ * head from float rows, encoded as dfv_kv_commit does (prefill).
  *
  *   src        device f32 or bf16 (src_dtype); element (row r, head h, dim
  *              c) at src[r * stride_row + h * stride_head + c] (elements)
- *   cache      device Q4_0 cache, written; ctx_len is not touched
+ *   cache      device cache in kv_format (DFV_KV_Q4_0 or DFV_KV_F16),
+ *              written; ctx_len is not touched
  * ---------------------------------------------------------------------- */
 dfv_status dfv_kv_quantize_rows(int n_kv_heads, int head_dim, int kv_format, int cache_capacity,
                                 int pos0, int n_rows, const void* src, int src_dtype,
@@ -250,10 +267,14 @@ dfv_status dfv_kv_quantize_rows(int n_kv_heads, int head_dim, int kv_format, int
 
 /* ------------------------------------------------------------------------
  * dfv_verify_step -- one whole greedy tree-verify step (attention, argmax +
- * walk, commit) in ONE cooperative kernel launch on `stream`: one CTA per SM,
- * one grid-wide barrier between the streaming / tensor-core phase and the
- * merge / walk / commit phase. Arguments and results as in the three entry
- * points above; the committed length advances by the accept length.
+ * walk, commit) in ONE cooperative kernel launch on `stream`: one CTA per SM.
+ * A split of the attention waits only for the other splits of its group
+ * before merging, and the walker waits only until every CTA has read the
+ * committed length and reported its argmax partials. Arguments and results
+ * as in the three entry points above (kv_format as for
+ * dfv_tree_verify_attn: the flag changes what the attention sees, the commit
+ * writes the cache format); the committed length advances by the accept
+ * length. The workspace size covers either cache format.
  * `workspace` (dfv_verify_step_workspace_bytes) must be zeroed once before
  * its first use; each call leaves it ready for the next. Calls sharing a
  * workspace must not overlap on the GPU.

@@ -25,11 +25,12 @@ Sources (cited by page title and section throughout):
 Module map:
 
 * ``q4_0``      -- Q4_0 block quantise / dequantise (fp32 rule, exact).
+* ``f16``       -- the binary16 (F16) cache format.
 * ``tree``      -- depth and ancestor sets of a draft tree.
 * ``attention`` -- tree-masked softmax attention, fp64, straight from the
                    definition (no flash / split-K restructuring).
 * ``accept``    -- per-node argmax and the greedy tree walk.
-* ``commit``    -- Q4_0 commit of the accepted rows into the cache.
+* ``commit``    -- commit of the accepted rows into the cache (Q4_0 or F16).
 * ``step``      -- the whole verify step composed from the above.
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
@@ -38,4 +39,4 @@ with the pages' own implementation is unpinned: the pages print no worked
 example and no kernel output.
 """
 
-from . import q4_0, tree, attention, accept, commit, step  # noqa: F401
+from . import q4_0, f16, tree, attention, accept, commit, step  # noqa: F401

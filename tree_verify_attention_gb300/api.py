@@ -11,7 +11,10 @@ from . import _lib
 
 DTYPE_F32 = 0
 DTYPE_BF16 = 1
+KV_F16 = 1
 KV_Q4_0 = 2
+KV_TREE_AS_CACHE = 0x100
+_FORMATS = {"q4_0": KV_Q4_0, "f16": KV_F16}
 MAX_NODES = 65
 
 DEV_BAD_TREE = 0x1
@@ -66,30 +69,55 @@ def q4_0_row_bytes(head_dim):
     return head_dim // 32 * 18
 
 
-class Q4Cache:
-    """Device Q4_0 KV cache of one sequence: K and V byte tensors
-    [Hkv, capacity, D/32 * 18] and the committed length (device int32)."""
+def row_bytes(head_dim, fmt="q4_0"):
+    """Bytes of one cache row (one KV head, one position)."""
+    if fmt == "f16":
+        return head_dim * 2
+    return q4_0_row_bytes(head_dim)
 
-    def __init__(self, n_kv_heads, head_dim, capacity, device="cuda"):
+
+def _fmt_code(fmt):
+    if fmt not in _FORMATS:
+        raise DfvError(f"unknown cache format {fmt!r} (expected one of {sorted(_FORMATS)})")
+    return _FORMATS[fmt]
+
+
+class KVCache:
+    """Device KV cache of one sequence in format ``fmt`` ("q4_0" or "f16"):
+    K and V byte tensors [Hkv, capacity, row bytes] and the committed length
+    (device int32)."""
+
+    def __init__(self, n_kv_heads, head_dim, capacity, device="cuda", fmt="q4_0"):
         self.n_kv_heads, self.head_dim, self.capacity = n_kv_heads, head_dim, capacity
-        shape = (n_kv_heads, capacity, q4_0_row_bytes(head_dim))
+        self.fmt = fmt
+        self.kv_format = _fmt_code(fmt)
+        shape = (n_kv_heads, capacity, row_bytes(head_dim, fmt))
         self.k = torch.zeros(shape, dtype=torch.uint8, device=device)
         self.v = torch.zeros(shape, dtype=torch.uint8, device=device)
         self.ctx_len = torch.zeros(1, dtype=torch.int32, device=device)
 
     def fill(self, k_rows, v_rows, pos0=0, stream=None):
-        """Quantise float rows [Hkv, n, D] (f32 or bf16) into positions
+        """Encode float rows [Hkv, n, D] (f32 or bf16) into positions
         [pos0, pos0 + n) and set the committed length to pos0 + n."""
         n = k_rows.shape[1]
         for src, dst in ((k_rows, self.k), (v_rows, self.v)):
             kv_quantize_rows(dst, src, pos0, self.n_kv_heads, self.head_dim, self.capacity,
-                             head_major=True, stream=stream)
+                             head_major=True, stream=stream, fmt=self.fmt)
         self.ctx_len.fill_(pos0 + n)
 
 
+class Q4Cache(KVCache):
+    """Device Q4_0 KV cache of one sequence: K and V byte tensors
+    [Hkv, capacity, D/32 * 18] and the committed length (device int32)."""
+
+    def __init__(self, n_kv_heads, head_dim, capacity, device="cuda"):
+        super().__init__(n_kv_heads, head_dim, capacity, device=device, fmt="q4_0")
+
+
 def kv_quantize_rows(cache, src, pos0, n_kv_heads, head_dim, capacity, head_major=False,
-                     stream=None):
-    """Quantise rows of ``src`` into ``cache`` positions [pos0, pos0 + n).
+                     stream=None, fmt="q4_0"):
+    """Encode rows of ``src`` into ``cache`` positions [pos0, pos0 + n) in
+    format ``fmt`` ("q4_0" or "f16").
     ``src`` is [n, Hkv, D] (or [Hkv, n, D] with head_major=True), f32 or
     bf16, last axis contiguous."""
     if src.dtype not in (torch.float32, torch.bfloat16) or not src.is_cuda:
@@ -102,7 +130,7 @@ def kv_quantize_rows(cache, src, pos0, n_kv_heads, head_dim, capacity, head_majo
         n, s_row, s_head = src.shape[0], src.stride(0), src.stride(1)
     dt = DTYPE_F32 if src.dtype == torch.float32 else DTYPE_BF16
     _dev(cache, "cache", (torch.uint8,))
-    _check(lib().dfv_kv_quantize_rows(n_kv_heads, head_dim, KV_Q4_0, capacity, pos0, n,
+    _check(lib().dfv_kv_quantize_rows(n_kv_heads, head_dim, _fmt_code(fmt), capacity, pos0, n,
                                       src.data_ptr(), dt, s_row, s_head, cache.data_ptr(),
                                       _stream(stream)), "dfv_kv_quantize_rows")
 
@@ -135,7 +163,7 @@ def workspace(nbytes, device="cuda", stream=None):
 
 
 def tree_verify_attn(cache, q, tree_k, tree_v, parent, window, max_depth, out, lse, ws,
-                     scale=0.0, status=None, stream=None):
+                     scale=0.0, status=None, stream=None, tree_as_cache=False):
     n, hq, d = q.shape
     hkv = tree_k.shape[1]
     _dev(q, "q", _BF16)
@@ -145,8 +173,9 @@ def tree_verify_attn(cache, q, tree_k, tree_v, parent, window, max_depth, out, l
     _dev(out, "out", _F32, n * hq * d)
     if lse is not None:
         _dev(lse, "lse", _F32, n * hq)
+    kvf = cache.kv_format | (KV_TREE_AS_CACHE if tree_as_cache else 0)
     _check(lib().dfv_tree_verify_attn(
-        n, max_depth, hq, hkv, d, window, KV_Q4_0, cache.capacity, cache.ctx_len.data_ptr(),
+        n, max_depth, hq, hkv, d, window, kvf, cache.capacity, cache.ctx_len.data_ptr(),
         cache.k.data_ptr(), cache.v.data_ptr(), q.data_ptr(), tree_k.data_ptr(),
         tree_v.data_ptr(), parent.data_ptr(), float(scale), out.data_ptr(), _p(lse),
         ws.data_ptr(), ws.numel(), _p(status), _stream(stream)), "dfv_tree_verify_attn")
@@ -174,7 +203,7 @@ def kv_commit(cache, accept_len, path, tree_k, tree_v, status=None, stream=None)
     _dev(accept_len, "accept_len", _I32, 1)
     _dev(path, "path", _I32)
     _check(lib().dfv_kv_commit(
-        n, cache.n_kv_heads, cache.head_dim, KV_Q4_0, cache.capacity, cache.ctx_len.data_ptr(),
+        n, cache.n_kv_heads, cache.head_dim, cache.kv_format, cache.capacity, cache.ctx_len.data_ptr(),
         accept_len.data_ptr(), path.data_ptr(), tree_k.data_ptr(), tree_v.data_ptr(),
         cache.k.data_ptr(), cache.v.data_ptr(), _p(status), _stream(stream)), "dfv_kv_commit")
 
@@ -201,7 +230,8 @@ class VerifyStep:
             raise DfvError(f"unsupported step shape {self.shape}")
         self.ws = workspace(nb, device=dev)
 
-    def run(self, cache, q, tree_k, tree_v, parent, tokens, logits, scale=0.0, stream=None):
+    def run(self, cache, q, tree_k, tree_v, parent, tokens, logits, scale=0.0, stream=None,
+            tree_as_cache=False):
         n, hq, hkv, d, window, cap, vocab = self.shape
         if cache.capacity != cap:
             raise DfvError("cache capacity differs from the planned one")
@@ -212,8 +242,9 @@ class VerifyStep:
         _dev(tokens, "tokens", _I32, n)
         _dev(logits, "logits", (torch.float32,) + _BF16, n * vocab)
         dt = DTYPE_F32 if logits.dtype == torch.float32 else DTYPE_BF16
+        kvf = cache.kv_format | (KV_TREE_AS_CACHE if tree_as_cache else 0)
         _check(lib().dfv_verify_step(
-            n, self.max_depth, hq, hkv, d, window, KV_Q4_0, cap, vocab, dt,
+            n, self.max_depth, hq, hkv, d, window, kvf, cap, vocab, dt,
             cache.ctx_len.data_ptr(), cache.k.data_ptr(), cache.v.data_ptr(), q.data_ptr(),
             tree_k.data_ptr(), tree_v.data_ptr(), parent.data_ptr(), tokens.data_ptr(),
             logits.data_ptr(), float(scale), self.out.data_ptr(), self.lse.data_ptr(),

@@ -135,7 +135,9 @@ __device__ __forceinline__ void q4_0_block_to_half(const uint16_t* codes, __half
 // Quantise 32 float values to one Q4_0 block with the binary32 rule:
 // m = first element of largest magnitude, d = m / -8, id = 1/d (0 if d = 0),
 // code = min(15, trunc(RN(RN(x * id) + 8.5))); scale stored as fp16 RN(d).
-__device__ __forceinline__ void q4_0_quantize_block(const float* x, uint8_t* blk) {
+// Results in registers: the 16 code bytes as four little-endian words (byte
+// j = code j | code j+16 << 4) and the fp16 scale bits.
+__device__ __forceinline__ void q4_0_quantize_regs(const float* x, uint32_t* code, uint32_t& dbits) {
   float amax = -1.0f, m = 0.0f;
 #pragma unroll
   for (int k = 0; k < 32; ++k) {
@@ -144,22 +146,67 @@ __device__ __forceinline__ void q4_0_quantize_block(const float* x, uint8_t* blk
   }
   const float d = __fdiv_rn(m, -8.0f);
   const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
-  uint8_t q[32];
+  uint32_t q[32];
 #pragma unroll
   for (int k = 0; k < 32; ++k) {
     const float t = __fadd_rn(__fmul_rn(x[k], id), 8.5f);
     const int c = __float2int_rz(t);
-    q[k] = static_cast<uint8_t>(c < 15 ? c : 15);
+    q[k] = static_cast<uint32_t>(c < 15 ? c : 15);
   }
-  const __half dh = __float2half_rn(d);
-  uint16_t* w = reinterpret_cast<uint16_t*>(blk);   // blocks are 2-byte aligned
-  w[0] = __half_as_ushort(dh);
+  dbits = __half_as_ushort(__float2half_rn(d));
 #pragma unroll
-  for (int j = 0; j < 16; j += 2) {
-    const uint32_t b0 = q[j] | (q[j + 16] << 4);
-    const uint32_t b1 = q[j + 1] | (q[j + 17] << 4);
-    w[1 + j / 2] = static_cast<uint16_t>(b0 | (b1 << 8));
+  for (int w = 0; w < 4; ++w) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int j = 4 * w + b;
+      word |= (q[j] | (q[j + 16] << 4)) << (8 * b);
+    }
+    code[w] = word;
   }
+}
+
+// The same block written as 18 bytes (fp16 scale, then the 16 code bytes).
+__device__ __forceinline__ void q4_0_quantize_block(const float* x, uint8_t* blk) {
+  uint32_t code[4], dbits;
+  q4_0_quantize_regs(x, code, dbits);
+  uint16_t* w = reinterpret_cast<uint16_t*>(blk);   // blocks are 2-byte aligned
+  w[0] = static_cast<uint16_t>(dbits);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    w[1 + 2 * k] = static_cast<uint16_t>(code[k] & 0xFFFFu);
+    w[2 + 2 * k] = static_cast<uint16_t>(code[k] >> 16);
+  }
+}
+
+// 16-byte asynchronous copy global -> shared (L2 only), and the wait for
+// this thread's copies (they then are visible to the thread).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// Eight bf16 values (16 bytes) as eight binary16 values, each rounded to
+// nearest even (exact for bf16 values in the binary16 normal range).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8_rn(uint4 v) {
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v);
+  uint4 o;
+  uint32_t* ov = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __bfloat1622float2(b[e]);
+    const __half2 h = __floats2half2_rn(f.x, f.y);
+    ov[e] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return o;
+}
+
+// Bytes of one cache row (one KV head, one position) of D values.
+__host__ __device__ constexpr int kv_row_bytes(int fmt, int D) {
+  return fmt == DFV_KV_F16 ? D * 2 : D / 32 * 18;
 }
 
 // ---------------------------------------------------------------- host helpers

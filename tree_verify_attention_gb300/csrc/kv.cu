@@ -1,13 +1,17 @@
-// Q4_0 commit of the accepted K/V rows, and Q4_0 prefill of cache rows.
+// Commit of the accepted K/V rows, and prefill of cache rows, in the Q4_0 or
+// the F16 cache format.
 //
 // "We got 207 tok/s with Qwen3.5-27B on an RTX 3090" (nowletus), "What we
-// ported and tuned": Q4_0 KV cache. After greedy acceptance the accepted
-// nodes' K/V rows are re-quantised into the cache at positions C .. C+L-1
-// and the committed length advances; rejected rows are never written.
+// ported and tuned": Q4_0 KV cache; "Luce DFlash ..." (ai-navigate-news, ja),
+// results paragraph: the F16 cache it is compared against. After greedy
+// acceptance the accepted nodes' K/V rows are encoded into the cache at
+// positions C .. C+L-1 and the committed length advances; rejected rows are
+// never written.
 //
 // The commit moves at most (budget + 1) rows per KV head; it runs as one
 // CTA so that reading C, writing the rows and advancing C need no
-// inter-CTA ordering. One thread quantises one 32-value block.
+// inter-CTA ordering. One thread encodes one 32-value Q4_0 block, or eight
+// values as binary16.
 
 #include "common.cuh"
 
@@ -16,7 +20,7 @@ namespace dfv {
 constexpr int kCommitThreads = 512;
 
 struct CommitParams {
-  int n_nodes, n_kv_heads, head_dim, capacity;
+  int n_nodes, n_kv_heads, head_dim, capacity, fmt;
   int32_t* ctx_len;
   const int32_t* accept_len;
   const int32_t* path;
@@ -65,8 +69,27 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(CommitParams p) 
   }
   __syncthreads();
   if (!s_ok) return;
+  const size_t row_bytes = static_cast<size_t>(kv_row_bytes(p.fmt, p.head_dim));
+  if (p.fmt == DFV_KV_F16) {
+    // eight values (16 bytes of bf16 -> 16 bytes of binary16) per item
+    const int np = p.head_dim / 8;
+    const int total = L * p.n_kv_heads * 2 * np;
+    for (int it = threadIdx.x; it < total; it += kCommitThreads) {
+      const int c = it % np;
+      const int kv = (it / np) & 1;
+      const int h = (it / (2 * np)) % p.n_kv_heads;
+      const int k = it / (2 * np * p.n_kv_heads);
+      const uint4 v = *reinterpret_cast<const uint4*>(
+          (kv ? p.tree_v : p.tree_k) + (static_cast<size_t>(s_path[k]) * p.n_kv_heads + h) * p.head_dim + c * 8);
+      *reinterpret_cast<uint4*>((kv ? p.v_cache : p.k_cache) +
+                                (static_cast<size_t>(h) * p.capacity + C + k) * row_bytes + c * 16) =
+          bf16x8_to_f16x8_rn(v);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) *p.ctx_len = C + L;
+    return;
+  }
   const int nb = p.head_dim / 32;
-  const size_t row_bytes = static_cast<size_t>(nb) * 18;
   const int total = L * p.n_kv_heads * 2 * nb;
   for (int it = threadIdx.x; it < total; it += kCommitThreads) {
     const int b = it % nb;
@@ -87,11 +110,39 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(CommitParams p) 
 }
 
 struct QuantRowsParams {
-  int n_kv_heads, head_dim, capacity, pos0, n_rows;
+  int n_kv_heads, head_dim, capacity, pos0, n_rows, fmt;
   const void* src;
   int64_t stride_row, stride_head;
   uint8_t* cache;
 };
+
+// F16 prefill: eight values per thread item, each rounded to binary16
+// (nearest even).
+template <typename T>
+__global__ void __launch_bounds__(256) f16_rows_kernel(QuantRowsParams p) {
+  const int np = p.head_dim / 8;
+  const size_t row_bytes = static_cast<size_t>(p.head_dim) * 2;
+  const int64_t total = static_cast<int64_t>(p.n_rows) * p.n_kv_heads * np;
+  const T* src = static_cast<const T*>(p.src);
+  for (int64_t it = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; it < total;
+       it += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(it % np);
+    const int h = static_cast<int>((it / np) % p.n_kv_heads);
+    const int64_t r = it / (static_cast<int64_t>(np) * p.n_kv_heads);
+    const T* s = src + r * p.stride_row + h * p.stride_head + c * 8;
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float a, b;
+      if constexpr (sizeof(T) == 4) { a = s[2 * k]; b = s[2 * k + 1]; }
+      else { a = __bfloat162float(s[2 * k]); b = __bfloat162float(s[2 * k + 1]); }
+      const __half2 hv = __floats2half2_rn(a, b);
+      w[k] = *reinterpret_cast<const uint32_t*>(&hv);
+    }
+    *reinterpret_cast<uint4*>(p.cache + (static_cast<size_t>(h) * p.capacity + p.pos0 + r) * row_bytes +
+                              c * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
 
 template <typename T>
 __global__ void __launch_bounds__(256) quantize_rows_kernel(QuantRowsParams p) {
@@ -120,7 +171,7 @@ dfv_status commit_launch(int n_nodes, int n_kv_heads, int head_dim, int kv_forma
                          int capacity, int32_t* ctx_len, const int32_t* accept_len,
                          const int32_t* path, const void* tree_k, const void* tree_v,
                          void* k_cache, void* v_cache, uint32_t* status, cudaStream_t stream) {
-  if (kv_format != DFV_KV_Q4_0) return DFV_ERR_UNSUPPORTED;
+  if (kv_format != DFV_KV_Q4_0 && kv_format != DFV_KV_F16) return DFV_ERR_UNSUPPORTED;
   if (n_nodes < 1 || n_nodes > kMaxNodes || n_kv_heads < 1 || capacity < 0)
     return DFV_ERR_INVALID;
   if (head_dim != 64 && head_dim != 128 && head_dim != 256) return DFV_ERR_UNSUPPORTED;
@@ -134,6 +185,7 @@ dfv_status commit_launch(int n_nodes, int n_kv_heads, int head_dim, int kv_forma
   p.n_kv_heads = n_kv_heads;
   p.head_dim = head_dim;
   p.capacity = capacity;
+  p.fmt = kv_format;
   p.ctx_len = ctx_len;
   p.accept_len = accept_len;
   p.path = path;
@@ -164,7 +216,7 @@ extern "C" dfv_status dfv_kv_quantize_rows(int n_kv_heads, int head_dim, int kv_
                                            int64_t stride_head, void* cache,
                                            dfv_stream_t stream) {
   using namespace dfv;
-  if (kv_format != DFV_KV_Q4_0) return DFV_ERR_UNSUPPORTED;
+  if (kv_format != DFV_KV_Q4_0 && kv_format != DFV_KV_F16) return DFV_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128 && head_dim != 256) return DFV_ERR_UNSUPPORTED;
   if (src_dtype != DFV_DTYPE_F32 && src_dtype != DFV_DTYPE_BF16) return DFV_ERR_UNSUPPORTED;
   if (n_kv_heads < 1 || cache_capacity < 0 || pos0 < 0 || n_rows < 0 ||
@@ -178,18 +230,26 @@ extern "C" dfv_status dfv_kv_quantize_rows(int n_kv_heads, int head_dim, int kv_
   p.capacity = cache_capacity;
   p.pos0 = pos0;
   p.n_rows = n_rows;
+  p.fmt = kv_format;
   p.src = src;
   p.stride_row = stride_row;
   p.stride_head = stride_head;
   p.cache = static_cast<uint8_t*>(cache);
-  const int64_t total = static_cast<int64_t>(n_rows) * n_kv_heads * (head_dim / 32);
+  const int per = kv_format == DFV_KV_F16 ? head_dim / 8 : head_dim / 32;   // thread items per row
+  const int64_t total = static_cast<int64_t>(n_rows) * n_kv_heads * per;
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = static_cast<int64_t>(sm_count()) * 16;
   if (blocks > cap) blocks = cap;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (src_dtype == DFV_DTYPE_F32)
+  if (kv_format == DFV_KV_F16) {
+    if (src_dtype == DFV_DTYPE_F32)
+      f16_rows_kernel<float><<<static_cast<int>(blocks), 256, 0, s>>>(p);
+    else
+      f16_rows_kernel<__nv_bfloat16><<<static_cast<int>(blocks), 256, 0, s>>>(p);
+  } else if (src_dtype == DFV_DTYPE_F32) {
     quantize_rows_kernel<float><<<static_cast<int>(blocks), 256, 0, s>>>(p);
-  else
+  } else {
     quantize_rows_kernel<__nv_bfloat16><<<static_cast<int>(blocks), 256, 0, s>>>(p);
+  }
   return cudaGetLastError() == cudaSuccess ? DFV_OK : DFV_ERR_CUDA;
 }

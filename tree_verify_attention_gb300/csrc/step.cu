@@ -67,6 +67,7 @@ struct StepParams {
   int lstride;       // bytes between staged slices
   uint32_t group_m;  // ceil(2^32 / group) (0 when group == 1): row -> node by multiply-high
   int do_accept;
+  int tree_q;        // attend Q4_0-quantised-and-dequantised tree rows
   int walker;        // CTA that merges the argmax partials, walks and commits
   int walker_local;  // 1: it quantises the tree rows into its own smem
   float scale_log2;
@@ -325,10 +326,24 @@ __device__ __noinline__ void plain_slices(const StepParams& p, int blk, int G) {
 
 // Q4_0 blocks [b0, b1) of the tree's key / value rows, laid out
 // [node][Hkv][K, V][row bytes] at qdst.
-template <int D>
+template <int D, int FMT>
 __device__ __noinline__ void prequant_tree(const StepParams& p, uint8_t* qdst, int b0, int b1) {
   constexpr int NB = D / 32;
-  constexpr int kRowB = StepSmem<D>::kRowB;
+  constexpr int kRowB = kv_row_bytes(FMT, D);
+  if constexpr (FMT == DFV_KV_F16) {
+    // items of eight values: bf16 -> binary16 (nearest even); b0, b1 count
+    // 32-value blocks, four items each
+    for (int it = 4 * b0 + static_cast<int>(threadIdx.x); it < 4 * b1; it += kStepThreads) {
+      const int c = it % (D / 8);
+      const int kv = (it / (D / 8)) & 1;
+      const int hh = (it / (2 * (D / 8))) % p.hkv;
+      const int t = it / (2 * (D / 8) * p.hkv);
+      const uint4 v = *reinterpret_cast<const uint4*>(
+          (kv ? p.tree_v : p.tree_k) + (static_cast<size_t>(t) * p.hkv + hh) * D + c * 8);
+      *reinterpret_cast<uint4*>(qdst + ((static_cast<size_t>(t) * p.hkv + hh) * 2 + kv) * kRowB + c * 16) =
+          bf16x8_to_f16x8_rn(v);
+    }
+  } else {
   for (int it = b0 + static_cast<int>(threadIdx.x); it < b1; it += kStepThreads) {
     const int b = it % NB;
     const int kv = (it / NB) & 1;
@@ -352,12 +367,13 @@ __device__ __noinline__ void prequant_tree(const StepParams& p, uint8_t* qdst, i
     }
     q4_0_quantize_block(x, qdst + ((static_cast<size_t>(t) * p.hkv + hh) * 2 + kv) * kRowB + b * 18);
   }
+  }
 }
 
 // The walker: waits until every other CTA has read ctx and written what it
 // owes (argmax partials, tree rows), merges the argmax partials per node,
 // walks the tree from the root and commits the accepted rows to the cache.
-template <int D>
+template <int D, int FMT>
 __device__ __noinline__ void walker_tail(const StepParams& p, int G, int C, uint8_t* sQ, const uint8_t* sK,
                                          const int* s_wpar, const int* s_wtok) {
   using L = StepSmem<D>;
@@ -452,16 +468,17 @@ __device__ __noinline__ void walker_tail(const StepParams& p, int G, int C, uint
   if (Cc + Lc > p.capacity) {
     if (tid == 0) report(p.status, DFV_DEV_CAPACITY);
   } else {
-    constexpr int W4 = L::kRowB / 4;
+    constexpr int kCRowB = kv_row_bytes(FMT, D);   // bytes of one cache row
+    constexpr int W4 = kCRowB / 4;
     const int total = Lc * p.hkv * 2 * W4;
     for (int it = tid; it < total; it += kStepThreads) {
       const int w = it % W4;
       const int kv = (it / W4) & 1;
       const int hh = (it / (2 * W4)) % p.hkv;
       const int k = it / (2 * W4 * p.hkv);
-      const size_t so = ((static_cast<size_t>(s_path[k]) * p.hkv + hh) * 2 + kv) * L::kRowB;
+      const size_t so = ((static_cast<size_t>(s_path[k]) * p.hkv + hh) * 2 + kv) * kCRowB;
       uint32_t* dst = reinterpret_cast<uint32_t*>(
-          (kv ? p.v_cache : p.k_cache) + (static_cast<size_t>(hh) * p.capacity + Cc + k) * L::kRowB);
+          (kv ? p.v_cache : p.k_cache) + (static_cast<size_t>(hh) * p.capacity + Cc + k) * kCRowB);
       dst[w] = p.walker_local ? reinterpret_cast<const uint32_t*>(sK + so)[w]
                               : __ldcg(reinterpret_cast<const uint32_t*>(p.qrows + so) + w);
     }
@@ -470,9 +487,10 @@ __device__ __noinline__ void walker_tail(const StepParams& p, int G, int C, uint
   }
 }
 
-template <int D, typename LT>
+template <int D, typename LT, int FMT>
 __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_constant__ StepParams p) {
   using L = StepSmem<D>;
+  constexpr bool kQ4 = FMT == DFV_KV_Q4_0;   // else binary16 cache rows
   constexpr int NB = D / 32;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // swizzle atoms need 1024-byte aligned bases; the launch adds 1 KB of slack
@@ -631,7 +649,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     }
     s_C = C;
     derive();
-    if constexpr (L::kBulk) {
+    if constexpr (L::kBulk && kQ4) {
       if (first_kv) issue_kv(c0);
     }
     // the logits copies go after the K/V copy, which is on the critical path
@@ -746,7 +764,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     if (mine) {
       const int nq = p.walker_local ? 1 : G;
       const int bq = p.walker_local ? 0 : blk;
-      prequant_tree<D>(p, qdst, static_cast<int>(static_cast<long>(bq) * tot / nq),
+      prequant_tree<D, FMT>(p, qdst, static_cast<int>(static_cast<long>(bq) * tot / nq),
                        static_cast<int>(static_cast<long>(bq + 1) * tot / nq));
     }
   }
@@ -790,7 +808,22 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       const bool committed = cc < n_cc;
       const int j0 = lo_min + cc * kChunk;
       const int nk = committed ? min(kChunk, C - j0) : 0;
-      if (committed) {
+      if (committed && !kQ4) {
+        // binary16 cache rows are MMA operands as they are: each thread copies
+        // its 16-byte pieces of the K and V rows straight into their
+        // swizzled slots; rows past the chunk's keys are zero
+        constexpr int PR = D / 8;                         // pieces per row
+        const uint8_t* kb = p.k_cache + (static_cast<size_t>(h) * p.capacity + j0) * (D * 2);
+        const uint8_t* vb = p.v_cache + (static_cast<size_t>(h) * p.capacity + j0) * (D * 2);
+        for (int it = tid; it < 2 * kChunk * PR; it += kStepThreads) {
+          const int kvi = it / (kChunk * PR), rem = it % (kChunk * PR);
+          const int key = rem / PR, c = rem % PR;
+          uint8_t* dst = (kvi ? sV : sK) + tc::sw128_offset(key, c, kChunk);
+          if (key < nk) cp_async16(dst, (kvi ? vb : kb) + key * (D * 2) + c * 16);
+          else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        cp_async_wait_all();
+      } else if (committed) {
         if constexpr (L::kBulk) {
           if (tid == 0 && !(i == 0 && first_kv)) issue_kv(cc);
           if (!cta_wait(bar_kv, ph_kv, &s_ok, p.status)) { alive = false; break; }
@@ -850,24 +883,56 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         // were loaded at entry.
         const int nt = nt_all;
         const int real = tree_real;
+        if (kQ4 && p.tree_q) {
+          // the tree rows as the commit stores them: each 32-value block is
+          // quantised to Q4_0 (the commit's rule) and dequantised again
+          constexpr int NB = D / 32;
+#pragma unroll 1
+          for (int it = tid; it < 2 * nt * NB; it += kStepThreads) {
+            const int ka = it / NB, b = it % NB;
+            const int kvi = ka >= nt ? 1 : 0, key = ka - kvi * nt;
+            const uint4* src = reinterpret_cast<const uint4*>(
+                (kvi ? p.tree_v : p.tree_k) + (static_cast<size_t>(key) * p.hkv + h) * D + b * 32);
+            float x[32];
 #pragma unroll
-        for (int u = 0; u < TP; ++u) {
-          const int it = tid + u * kStepThreads;
-          if (it < real) {
+            for (int u4 = 0; u4 < 4; ++u4) {
+              const uint4 r4 = __ldg(src + u4);
+              const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&r4);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(hb[e]);
+                x[u4 * 8 + 2 * e] = f.x;
+                x[u4 * 8 + 2 * e + 1] = f.y;
+              }
+            }
+            uint32_t code[4], dbits;
+            q4_0_quantize_regs(x, code, dbits);
+            uint4 o4[4];
+            q4_0_block_chunks(code, dbits, o4);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              *reinterpret_cast<uint4*>((kvi ? sV : sK) + tc::sw128_offset(key, b * 4 + e, kChunk)) = o4[e];
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < TP; ++u) {
+            const int it = tid + u * kStepThreads;
+            if (it < real) {
+              const int ka = it / (D / 8), c = it % (D / 8);
+              const int kvi = ka >= nt ? 1 : 0, key = ka - kvi * nt;
+              *reinterpret_cast<uint4*>((kvi ? sV : sK) + tc::sw128_offset(key, c, kChunk)) =
+                  bf16x8_to_f16x8(tv[u]);
+            }
+          }
+#pragma unroll 1
+          for (int it = tid + TP * kStepThreads; it < real; it += kStepThreads) {
             const int ka = it / (D / 8), c = it % (D / 8);
             const int kvi = ka >= nt ? 1 : 0, key = ka - kvi * nt;
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+                (kvi ? p.tree_v : p.tree_k) + (static_cast<size_t>(key) * p.hkv + h) * D + c * 8));
             *reinterpret_cast<uint4*>((kvi ? sV : sK) + tc::sw128_offset(key, c, kChunk)) =
-                bf16x8_to_f16x8(tv[u]);
+                bf16x8_to_f16x8(v);
           }
-        }
-#pragma unroll 1
-        for (int it = tid + TP * kStepThreads; it < real; it += kStepThreads) {
-          const int ka = it / (D / 8), c = it % (D / 8);
-          const int kvi = ka >= nt ? 1 : 0, key = ka - kvi * nt;
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-              (kvi ? p.tree_v : p.tree_k) + (static_cast<size_t>(key) * p.hkv + h) * D + c * 8));
-          *reinterpret_cast<uint4*>((kvi ? sV : sK) + tc::sw128_offset(key, c, kChunk)) =
-              bf16x8_to_f16x8(v);
         }
         const int zero = 2 * (kChunk - nt) * (D / 8);
         for (int it = tid; it < zero; it += kStepThreads) {
@@ -1090,7 +1155,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
   // ---- the walker: once every other CTA has read ctx and written its
   // argmax partial, merge the partials, walk and commit -- all before the
   // group barriers, under the attention of the other CTAs
-  if (p.do_accept && blk == p.walker) walker_tail<D>(p, G, C, sQ, sK, s_wpar, s_wtok);
+  if (p.do_accept && blk == p.walker) walker_tail<D, FMT>(p, G, C, sQ, sK, s_wpar, s_wtok);
 
   // ================================================================ merge
   // Each of the `splits` CTAs of a (KV head, row tile) group waits for the
@@ -1190,7 +1255,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
 static size_t a256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, int cap, int vocab,
-                      int logits_dtype, bool with_accept, StepPlan* pl) {
+                      int logits_dtype, bool with_accept, int kv_fmt, StepPlan* pl) {
   if (n_nodes < 1 || n_nodes > kMaxNodes || hkv < 1 || hq < hkv || hq % hkv || hq > 256 ||
       window < 0 || cap < 0)
     return false;
@@ -1331,7 +1396,7 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
     }
   }
   {
-    const long qbytes = static_cast<long>(n_nodes) * hkv * 2 * (head_dim / 32 * 18);
+    const long qbytes = static_cast<long>(n_nodes) * hkv * 2 * kv_row_bytes(kv_fmt, head_dim);
     const long room = static_cast<long>(kChunk) * (head_dim > kChunk ? head_dim : kChunk) * 2;  // sK
     pl->walker_local = with_accept && pl->grid > pl->units && qbytes <= room ? 1 : 0;
   }
@@ -1340,7 +1405,9 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
     case 128: pl->smem = StepSmem<128>::kBytes; break;
     default: pl->smem = StepSmem<256>::kBytes; break;
   }
-  const int rowb = head_dim / 32 * 18;
+  // staged tree rows: sized for the larger (binary16) row, so one workspace
+  // serves either cache format
+  const int rowb = kv_row_bytes(DFV_KV_F16, head_dim);
   pl->ws_bar = 0;
   pl->ws_arg = a256(static_cast<size_t>(4 + 2 * hkv * pl->n_mt + pl->units) * sizeof(unsigned int));
   pl->ws_qrows = pl->ws_arg + a256(static_cast<size_t>(pl->lunits) * sizeof(ArgPartial));
@@ -1351,17 +1418,17 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
   return true;
 }
 
-template <int D, typename LT>
+template <int D, typename LT, int FMT>
 static dfv_status step_launch_dt(StepParams& p, const StepPlan& pl, cudaStream_t stream) {
   static int configured[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DFV_ERR_CUDA;
   if (!configured[dev]) {
-    if (cudaFuncSetAttribute(step_kernel<D, LT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(step_kernel<D, LT, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              StepSmem<D>::kBytes) != cudaSuccess)
       return DFV_ERR_CUDA;
     int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, step_kernel<D, LT>, kStepThreads,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, step_kernel<D, LT, FMT>, kStepThreads,
                                                       StepSmem<D>::kBytes) != cudaSuccess ||
         nb < 1)
       return DFV_ERR_CUDA;
@@ -1377,24 +1444,32 @@ static dfv_status step_launch_dt(StepParams& p, const StepPlan& pl, cudaStream_t
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, step_kernel<D, LT>, p) == cudaSuccess ? DFV_OK : DFV_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, step_kernel<D, LT, FMT>, p) == cudaSuccess ? DFV_OK : DFV_ERR_CUDA;
 }
 
 // One instantiation per logits element type (the attention-only launch has
 // no logits and takes the bf16 one).
+template <int D, int FMT>
+static dfv_status step_launch_f(StepParams& p, const StepPlan& pl, cudaStream_t stream) {
+  if (p.do_accept && p.logits_dtype == DFV_DTYPE_F32) return step_launch_dt<D, float, FMT>(p, pl, stream);
+  return step_launch_dt<D, __nv_bfloat16, FMT>(p, pl, stream);
+}
+
 template <int D>
-static dfv_status step_launch_d(StepParams& p, const StepPlan& pl, cudaStream_t stream) {
-  if (p.do_accept && p.logits_dtype == DFV_DTYPE_F32) return step_launch_dt<D, float>(p, pl, stream);
-  return step_launch_dt<D, __nv_bfloat16>(p, pl, stream);
+static dfv_status step_launch_d(StepParams& p, const StepPlan& pl, int fmt, cudaStream_t stream) {
+  if (fmt == DFV_KV_F16) return step_launch_f<D, DFV_KV_F16>(p, pl, stream);
+  return step_launch_f<D, DFV_KV_Q4_0>(p, pl, stream);
 }
 
 // Workspace of either logits element size (the slicing differs slightly).
 size_t step_workspace_bytes(int n_nodes, int hq, int hkv, int head_dim, int window, int cap,
                             int vocab, bool with_accept) {
   StepPlan a, b;
-  if (!step_plan(n_nodes, hq, hkv, head_dim, window, cap, vocab, DFV_DTYPE_F32, with_accept, &a))
+  if (!step_plan(n_nodes, hq, hkv, head_dim, window, cap, vocab, DFV_DTYPE_F32, with_accept,
+                 DFV_KV_Q4_0, &a))
     return 0;
-  step_plan(n_nodes, hq, hkv, head_dim, window, cap, vocab, DFV_DTYPE_BF16, with_accept, &b);
+  step_plan(n_nodes, hq, hkv, head_dim, window, cap, vocab, DFV_DTYPE_BF16, with_accept, DFV_KV_Q4_0,
+            &b);
   return a.ws_total > b.ws_total ? a.ws_total : b.ws_total;
 }
 
@@ -1407,13 +1482,15 @@ dfv_status step_launch(bool with_accept, int n_nodes, int max_depth, int hq, int
                        float scale, float* out, float* lse, int32_t* argmax, int32_t* accept_len,
                        int32_t* path, int32_t* out_tokens, void* workspace, size_t ws_bytes,
                        uint32_t* status, cudaStream_t stream) {
-  if (kv_format != DFV_KV_Q4_0) return DFV_ERR_UNSUPPORTED;
+  const int fmt = kv_format & 0xFF, flags = kv_format & ~0xFF;
+  if ((fmt != DFV_KV_Q4_0 && fmt != DFV_KV_F16) || (flags & ~DFV_KV_TREE_AS_CACHE) != 0)
+    return DFV_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128 && head_dim != 256) return DFV_ERR_UNSUPPORTED;
   if (with_accept && logits_dtype != DFV_DTYPE_F32 && logits_dtype != DFV_DTYPE_BF16)
     return DFV_ERR_UNSUPPORTED;
   StepPlan pl;
   if (!step_plan(n_nodes, hq, hkv, head_dim, window, cap, vocab,
-                 with_accept ? logits_dtype : DFV_DTYPE_F32, with_accept, &pl))
+                 with_accept ? logits_dtype : DFV_DTYPE_F32, with_accept, fmt, &pl))
     return DFV_ERR_INVALID;
   if (!ctx_len || !k_cache || !v_cache || !q || !tree_k || !tree_v || !parent || !out || !workspace)
     return DFV_ERR_INVALID;
@@ -1445,6 +1522,9 @@ dfv_status step_launch(bool with_accept, int n_nodes, int max_depth, int hq, int
   p.lbulk = pl.lbulk;
   p.lstride = pl.lstride;
   p.do_accept = with_accept ? 1 : 0;
+  // binary16 tree rows are exact in the cache format, so the flag only
+  // changes anything for Q4_0
+  p.tree_q = (flags & DFV_KV_TREE_AS_CACHE) && fmt == DFV_KV_Q4_0 ? 1 : 0;
   p.walker = pl.walker;
   p.walker_local = pl.walker_local;
   for (int i = 0; i < kMaxStepGrid; ++i) p.lslot[i] = pl.lslot[i];
@@ -1474,9 +1554,9 @@ dfv_status step_launch(bool with_accept, int n_nodes, int max_depth, int hq, int
   p.part_o = reinterpret_cast<__half*>(ws + pl.ws_o);
   p.status = status;
   switch (head_dim) {
-    case 64: return step_launch_d<64>(p, pl, stream);
-    case 128: return step_launch_d<128>(p, pl, stream);
-    default: return step_launch_d<256>(p, pl, stream);
+    case 64: return step_launch_d<64>(p, pl, fmt, stream);
+    case 128: return step_launch_d<128>(p, pl, fmt, stream);
+    default: return step_launch_d<256>(p, pl, fmt, stream);
   }
 }
 
