@@ -49,6 +49,10 @@ def parse_args(argv=None):
     ap.add_argument("--replicas", type=int, default=REPLICAS, help="KV-cache replicas")
     ap.add_argument("--cpu-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--source-hash", action="store_true", help="print the kernel source hash")
+    ap.add_argument("--fmt", choices=["q4_0", "f16"], default="q4_0",
+                    help="KV-cache format (the headline workload is Q4_0)")
+    ap.add_argument("--tree-as-cache", action="store_true",
+                    help="attend the tree rows as the commit stores them")
     return ap.parse_args(argv)
 
 
@@ -215,20 +219,22 @@ class CacheView:
     """A replica's K/V byte tensors and committed length (views into the
     replica pool), shaped like api.Q4Cache."""
 
-    def __init__(self, k, v, ctx_len, n_kv_heads, head_dim, capacity):
+    def __init__(self, k, v, ctx_len, n_kv_heads, head_dim, capacity, fmt="q4_0"):
+        from tree_verify_attention_gb300 import api
         self.k, self.v, self.ctx_len = k, v, ctx_len
         self.n_kv_heads, self.head_dim, self.capacity = n_kv_heads, head_dim, capacity
-        self.fmt, self.kv_format = "q4_0", 2
+        self.fmt, self.kv_format = fmt, api._fmt_code(fmt)
 
 
-def algorithmic_per_step(cfg, parents):
+def algorithmic_per_step(cfg, parents, fmt="q4_0"):
     """KV bytes, logits bytes and attention flops one step must move / do,
     averaged over the step inputs (the flops depend on the tree only
     through the window bound, so they are equal for every input here)."""
     import numpy as np
+    from tree_verify_attention_gb300 import api
     D, hkv, hq, N, W_, C = (cfg.head_dim, cfg.n_kv_heads, cfg.n_q_heads, cfg.n_nodes,
                             cfg.window, cfg.ctx_len)
-    row = D // 32 * 18
+    row = api.row_bytes(D, fmt)
     kv_rows = min(W_ - 1, C) if W_ > 0 else C
     kv_bytes = kv_rows * row * 2 * hkv
     logits_bytes = N * cfg.vocab * 2
@@ -266,7 +272,7 @@ def run_gpu(args):
     per_phase = max(K, Wu, args.e2e_steps, args.probe_steps)
     n_pool, n_rep = args.pool, args.replicas
     cap = C + (math.ceil(per_phase / n_rep) + 2) * N
-    row = D // 32 * 18
+    row = api.row_bytes(D, args.fmt)
 
     # ---- inputs: step pool (independent per rank) and cache replicas
     seed_off = 1000 * rank
@@ -283,7 +289,7 @@ def run_gpu(args):
     lg_all = torch.stack([bf(s.logits) for s in steps_np]).to(dev)
 
     kf, vf = W.make_context(cfg, seed=cfg.seed + rank)
-    base = api.Q4Cache(hkv, D, cap, device=dev)
+    base = api.KVCache(hkv, D, cap, device=dev, fmt=args.fmt)
     base.fill(torch.from_numpy(kf).to(dev), torch.from_numpy(vf).to(dev))
     del kf, vf
     k_all = base.k.unsqueeze(0).repeat(n_rep, 1, 1, 1)
@@ -291,7 +297,8 @@ def run_gpu(args):
     ctx0 = torch.full((n_rep,), C, dtype=torch.int32, device=dev)
     ctx_all = ctx0.clone()
     del base
-    caches = [CacheView(k_all[r], v_all[r], ctx_all[r:r + 1], hkv, D, cap) for r in range(n_rep)]
+    caches = [CacheView(k_all[r], v_all[r], ctx_all[r:r + 1], hkv, D, cap, args.fmt)
+              for r in range(n_rep)]
 
     st = api.VerifyStep(N, hq, hkv, D, Wn, cap, V, max_depth=cfg.max_depth, device=dev)
     launches_per_step = api.step_launches(N, hq, hkv, D, Wn, cap)
@@ -299,7 +306,7 @@ def run_gpu(args):
     def one_step(i):
         j = i % n_pool
         st.run(caches[i % n_rep], q_all[j], tk_all[j], tv_all[j], par_all[j], tok_all[j],
-               lg_all[j])
+               lg_all[j], tree_as_cache=args.tree_as_cache)
 
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
@@ -376,7 +383,7 @@ def run_gpu(args):
     e2e = run_e2e(args, api, cfg, steps_np, caches, ctx_all, ctx0, st, stream, dev)
 
     status = int(st.status.item())
-    kv_b, lg_b, flops = algorithmic_per_step(cfg, [s.parent for s in steps_np])
+    kv_b, lg_b, flops = algorithmic_per_step(cfg, [s.parent for s in steps_np], args.fmt)
     ms = 1000.0 * slowest / K
     per_rank_sps = K / slowest
     kvlg_gbs = (kv_b + lg_b) * per_rank_sps / 1e9
@@ -420,7 +427,9 @@ def run_gpu(args):
             "vs_baseline": None, "dtype": "f16", "data": "synthetic",
             "config": {"workload": WORKLOAD, "ctx": C, "window": Wn, "budget": N - 1,
                        "heads": f"{hq}/{hkv}", "head_dim": D, "vocab": V, "logits": "bf16",
-                       "kv": "Q4_0", "tree": "random depth<=16, planted path 8, p=0.8",
+                       "kv": {"q4_0": "Q4_0", "f16": "F16"}[args.fmt]
+                             + (", tree rows as cached" if args.tree_as_cache else ""),
+                       "tree": "random depth<=16, planted path 8, p=0.8",
                        "l2": f"inputs > L2: {n_pool} step inputs x 7.4 MB and {n_rep} "
                              f"KV-cache replicas cycled", "graph": "one CUDA graph of K steps"},
             "kv_logits_bytes_per_step": kv_b + lg_b,
@@ -517,7 +526,8 @@ def run_e2e(args, api, cfg, steps_np, caches, ctx_all, ctx0, st, stream, dev):
         for d, h in ((d_q, h_q), (d_tk, h_tk), (d_tv, h_tv), (d_par, h_par), (d_tok, h_tok),
                      (d_lg, h_lg)):
             d.copy_(h[j], non_blocking=True)
-        st.run(caches[i % len(caches)], d_q, d_tk, d_tv, d_par, d_tok, d_lg)
+        st.run(caches[i % len(caches)], d_q, d_tk, d_tv, d_par, d_tok, d_lg,
+               tree_as_cache=args.tree_as_cache)
         h_out_tok[i].copy_(st.out_tokens, non_blocking=True)
         h_acc[i].copy_(st.accept_len, non_blocking=True)
 
