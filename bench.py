@@ -493,8 +493,12 @@ def _peaks():
 
 def run_e2e(args, api, cfg, steps_np, caches, ctx_all, ctx0, st, stream, dev):
     """Same steps through the public API with inputs in pinned host memory:
-    each step copies its inputs host -> device, runs, and copies the
-    accepted tokens back (one CUDA graph of the copies and launches)."""
+    every step copies its inputs host -> device, runs, and copies its
+    accepted tokens back. Two sets of device inputs and two step objects
+    (outputs + workspace) alternate, so that the copies of step i+1 (on a
+    copy-in stream) overlap the kernel of step i, and step i's results are
+    read back on a copy-out stream once its kernel is done. The kernels stay
+    in one stream, strictly in order. One CUDA graph holds all of it."""
     import numpy as np
     import torch
     n_steps = args.e2e_steps
@@ -504,37 +508,60 @@ def run_e2e(args, api, cfg, steps_np, caches, ctx_all, ctx0, st, stream, dev):
         t = torch.stack([torch.from_numpy(np.ascontiguousarray(a)) for a in arrs])
         return t.view(dtype).pin_memory() if dtype is not None else t.pin_memory()
 
-    h_q = pin([s.q.view(np.int16) for s in steps_np], torch.bfloat16)
-    h_tk = pin([s.k_tree.view(np.int16) for s in steps_np], torch.bfloat16)
-    h_tv = pin([s.v_tree.view(np.int16) for s in steps_np], torch.bfloat16)
-    h_par = pin([s.parent for s in steps_np], None)
-    h_tok = pin([s.tokens for s in steps_np], None)
-    h_lg = pin([s.logits.view(np.int16) for s in steps_np], torch.bfloat16)
-    d_q = torch.empty_like(h_q[0], device=dev)
-    d_tk = torch.empty_like(h_tk[0], device=dev)
-    d_tv = torch.empty_like(h_tv[0], device=dev)
-    d_par = torch.empty_like(h_par[0], device=dev)
-    d_tok = torch.empty_like(h_tok[0], device=dev)
-    d_lg = torch.empty_like(h_lg[0], device=dev)
+    h_in = [pin([s.q.view(np.int16) for s in steps_np], torch.bfloat16),
+            pin([s.k_tree.view(np.int16) for s in steps_np], torch.bfloat16),
+            pin([s.v_tree.view(np.int16) for s in steps_np], torch.bfloat16),
+            pin([s.parent for s in steps_np], None),
+            pin([s.tokens for s in steps_np], None),
+            pin([s.logits.view(np.int16) for s in steps_np], torch.bfloat16)]
+    d_in = [[torch.empty_like(h[0], device=dev) for h in h_in] for _ in range(2)]
+    steps = [st, api.VerifyStep(N, hq, hkv, D, cfg.window, st.shape[5], V,
+                                max_depth=st.max_depth, device=dev)]
     h_out_tok = torch.empty((n_steps, N), dtype=torch.int32).pin_memory()
     h_acc = torch.empty((n_steps, 1), dtype=torch.int32).pin_memory()
-    h2d = sum(t[0].numel() * t.element_size() for t in (h_q, h_tk, h_tv, h_par, h_tok, h_lg))
+    h2d = sum(h[0].numel() * h.element_size() for h in h_in)
     d2h = h_out_tok[0].numel() * 4 + 4
+    s_in = torch.cuda.Stream(device=dev)
+    s_out = torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(n_steps)]     # step i's inputs on the device
+    ev_done = [torch.cuda.Event() for _ in range(n_steps)]   # step i's kernel finished
+    ev_read = [torch.cuda.Event() for _ in range(n_steps)]   # step i's results read back
 
-    def one(i):
-        j = i % len(steps_np)
-        for d, h in ((d_q, h_q), (d_tk, h_tk), (d_tv, h_tv), (d_par, h_par), (d_tok, h_tok),
-                     (d_lg, h_lg)):
-            d.copy_(h[j], non_blocking=True)
-        st.run(caches[i % len(caches)], d_q, d_tk, d_tv, d_par, d_tok, d_lg,
-               tree_as_cache=args.tree_as_cache)
-        h_out_tok[i].copy_(st.out_tokens, non_blocking=True)
-        h_acc[i].copy_(st.accept_len, non_blocking=True)
+    def copy_in(i):
+        b, j = i % 2, i % len(steps_np)
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev_done[i - 2])      # buffer set b no longer read
+            for d, h in zip(d_in[b], h_in):
+                d.copy_(h[j], non_blocking=True)
+            ev_in[i].record(s_in)
+
+    def body():
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        copy_in(0)
+        for i in range(n_steps):
+            b = i % 2
+            if i + 1 < n_steps:
+                copy_in(i + 1)                       # overlaps step i's kernel
+            stream.wait_event(ev_in[i])
+            if i >= 2:
+                stream.wait_event(ev_read[i - 2])    # step object b's outputs read back
+            q, tk, tv, par, tok, lg = d_in[b]
+            steps[b].run(caches[i % len(caches)], q, tk, tv, par, tok, lg, stream=stream,
+                         tree_as_cache=args.tree_as_cache)
+            ev_done[i].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[i])
+                h_out_tok[i].copy_(steps[b].out_tokens, non_blocking=True)
+                h_acc[i].copy_(steps[b].accept_len, non_blocking=True)
+                ev_read[i].record(s_out)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
 
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
-        for i in range(n_steps):
-            one(i)
+        body()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
@@ -547,11 +574,18 @@ def run_e2e(args, api, cfg, steps_np, caches, ctx_all, ctx0, st, stream, dev):
         ev1.record(stream)
     torch.cuda.synchronize()
     t = ev0.elapsed_time(ev1) / 1000.0
+    acc = h_acc[:, 0].numpy()
+    if not ((acc >= 1) & (acc <= N)).all():
+        raise RuntimeError("end-to-end run read back an accept length outside [1, N]")
     _, world, _ = dist_env()
     value, _ = whole_job_value(t, n_steps, world, device=dev)
     return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": n_steps, "note": "pinned host inputs copied in and accepted tokens copied "
-                                      "out every step, inside one CUDA graph"}
+            "steps": n_steps, "device_status": int(steps[1].status.item()),
+            "mean_accept_len": float(acc.mean()),
+            "note": "pinned host inputs copied in and accepted tokens copied "
+                                      "out every step, inside one CUDA graph; step i+1's "
+                                      "copies overlap step i's kernel (two input sets), "
+                                      "kernels strictly in order"}
 
 
 def main(argv=None):
