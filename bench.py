@@ -53,6 +53,8 @@ def parse_args(argv=None):
                     help="KV-cache format (the headline workload is Q4_0)")
     ap.add_argument("--tree-as-cache", action="store_true",
                     help="attend the tree rows as the commit stores them")
+    ap.add_argument("--sweep", action="store_true",
+                    help="budget x tree-shape sweep at context 32768 (one JSON line per point)")
     return ap.parse_args(argv)
 
 
@@ -588,6 +590,86 @@ def run_e2e(args, api, cfg, steps_np, caches, ctx_all, ctx0, st, stream, dev):
                                       "kernels strictly in order"}
 
 
+def run_sweep(args):
+    """Budget x tree-shape sweep on the 32768-context workload (window 2048,
+    24/4 heads, D 256, vocabulary 151936 bf16, planted acceptance p = 0.8):
+    per point, GPU steps/s over a CUDA graph of strictly serial steps (inputs
+    cycled over 16 step inputs and 16 cache replicas), the mean accept length
+    of those inputs (the greedy walk of the oracle, which the kernel matches
+    bit for bit) and their product, accepted tokens/s. The pages found budget
+    22 the best trade-off on an RTX 3090 ("We got 207 tok/s ...", DFlash
+    section); this measures where it lies on this GPU."""
+    import numpy as np
+    import torch
+    import oracle
+    from tree_verify_attention_gb300 import api, build
+    from tree_verify_attention_gb300 import workload as W
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    points = [c for c in W.sweep_configs() if c.p_accept == 0.8 and c.seed == 0]
+    K, R, P = max(64, args.steps // 5), 16, 16
+    base_cfg = points[0]
+    C, hkv, hq, D, Wn, V = (base_cfg.ctx_len, base_cfg.n_kv_heads, base_cfg.n_q_heads,
+                            base_cfg.head_dim, base_cfg.window, base_cfg.vocab)
+    cap = C + (K // R + 2) * 65                 # room for every step's commit (N <= 65)
+    kf, vf = W.make_context(base_cfg)
+    base = api.KVCache(hkv, D, cap, device=dev, fmt=args.fmt)
+    base.fill(torch.from_numpy(kf).to(dev), torch.from_numpy(vf).to(dev))
+    del kf, vf
+    k_all = base.k.unsqueeze(0).repeat(R, 1, 1, 1)
+    v_all = base.v.unsqueeze(0).repeat(R, 1, 1, 1)
+    ctx0 = torch.full((R,), C, dtype=torch.int32, device=dev)
+    ctx_all = ctx0.clone()
+    caches = [CacheView(k_all[r], v_all[r], ctx_all[r:r + 1], hkv, D, cap, args.fmt) for r in range(R)]
+    stream = torch.cuda.Stream(device=dev)
+
+    def bf(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    for cfg in points:
+        N = cfg.n_nodes
+        pool = [W.make_step(cfg, i) for i in range(P)]
+        ins = [(bf(s.q), bf(s.k_tree), bf(s.v_tree), torch.from_numpy(s.parent).to(dev),
+                torch.from_numpy(s.tokens).to(dev), bf(s.logits)) for s in pool]
+        st = api.VerifyStep(N, hq, hkv, D, Wn, cap, V, max_depth=max(cfg.max_depth, 1), device=dev)
+        lens = []
+        for s in pool:
+            am = oracle.accept.node_argmax(W.bf16_bits_to_f32(s.logits))
+            lens.append(len(oracle.accept.greedy_walk(s.parent, s.tokens, am)[0]))
+
+        def one(i):
+            st.run(caches[i % R], *ins[i % P], stream=stream, tree_as_cache=args.tree_as_cache)
+
+        with torch.cuda.stream(stream):
+            for i in range(4):
+                one(i)
+            ctx_all.copy_(ctx0)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(K):
+                one(i)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                ctx_all.copy_(ctx0)
+                g.replay()
+            ctx_all.copy_(ctx0)
+            ev0.record(stream)
+            g.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize()
+        sps = K / (ev0.elapsed_time(ev1) / 1000.0)
+        mean_l = float(np.mean(lens))
+        print(json.dumps({"sweep": cfg.name, "budget": cfg.budget, "tree": cfg.tree, "p_accept": 0.8,
+                          "ctx": C, "window": Wn, "kv": args.fmt, "steps_per_s": sps,
+                          "us_per_step": 1e6 / sps, "mean_accept_len": mean_l,
+                          "accepted_tokens_per_s": sps * mean_l,
+                          "device_status": int(st.status.item())}), flush=True)
+        del g, st, ins
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.source_hash:
@@ -598,6 +680,9 @@ def main(argv=None):
         return
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.sweep:
+        run_sweep(args)
         return
     run_gpu(args)
 
