@@ -253,6 +253,71 @@ def algorithmic_per_step(cfg, parents, fmt="q4_0"):
     return kv_bytes, logits_bytes, float(np.mean(flops))
 
 
+def run_modes(args, api, cfg, caches, ctx_all, ctx0, q_all, tk_all, tv_all, par_all, tok_all,
+              lg_all, K, stream, dev):
+    """Steps/s of K chained steps in each dependency mode ("strict": a step
+    starts once the previous one has completed; "pipelined": it overlaps the
+    previous step, waiting only before it reads ctx and the cache) over cold
+    caches (the replicas, cycled) and over one hot cache (all steps on one
+    cache, whose window stays in L2). One CUDA graph of K steps each, replayed
+    once untimed and then timed with CUDA events."""
+    import torch
+    N, hq, hkv, D, Wn, V, C = (cfg.n_nodes, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim,
+                               cfg.window, cfg.vocab, cfg.ctx_len)
+    n_pool, n_rep, cap = q_all.shape[0], len(caches), caches[0].capacity
+    hot_cap = C + (K + 4) * N
+    hot = api.KVCache(hkv, D, hot_cap, device=dev, fmt=args.fmt)
+    hot.k[:, :cap].copy_(caches[0].k)
+    hot.v[:, :cap].copy_(caches[0].v)
+    hot_ctx0 = torch.full((1,), C, dtype=torch.int32, device=dev)
+    out = {}
+    for kv in ("cold", "hot"):
+        for dep in ("strict", "pipelined"):
+            c_cap = cap if kv == "cold" else hot_cap
+            st = api.VerifyStep(N, hq, hkv, D, Wn, c_cap, V, max_depth=cfg.max_depth, device=dev,
+                                pipelined=dep == "pipelined")
+
+            def reset():
+                if kv == "cold":
+                    ctx_all.copy_(ctx0)
+                else:
+                    hot.ctx_len.copy_(hot_ctx0)
+
+            def one(i):
+                j = i % n_pool
+                cache = caches[i % n_rep] if kv == "cold" else hot
+                st.run(cache, q_all[j], tk_all[j], tv_all[j], par_all[j], tok_all[j], lg_all[j],
+                       tree_as_cache=args.tree_as_cache)
+
+            with torch.cuda.stream(stream):
+                for i in range(3):          # eager: sets kernel attributes before capture
+                    one(i)
+                reset()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(K):
+                    one(i)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                reset()
+                g.replay()
+                reset()
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            t = e0.elapsed_time(e1) / 1000.0
+            out[f"{dep}_{kv}"] = {"steps_per_s": K / t, "us_per_step": 1e6 * t / K,
+                                  "device_status": int(st.status.item())}
+            del g, st
+    out["note"] = ("strict_cold is the headline's mode; pipelined = DFV_STEP_PIPELINED "
+                   "(programmatic dependent launch, two workspaces in turn); hot = one cache "
+                   "for all K steps")
+    return out
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -378,8 +443,15 @@ def run_gpu(args):
             one_step(Wu + i)
             evs[i][1].record(stream)
     torch.cuda.synchronize()
-    clk = clocks.stop()
     t_kernel = statistics.mean(a.elapsed_time(b) for a, b in evs) / 1000.0
+
+    # ---- the other dependency and KV modes (same step inputs, K steps each)
+    try:
+        modes = run_modes(args, api, cfg, caches, ctx_all, ctx0, q_all, tk_all, tv_all, par_all,
+                          tok_all, lg_all, K, stream, dev)
+    except Exception as ex:  # reported, not fatal to the headline
+        modes = {"error": f"{type(ex).__name__}: {ex}"[:300]}
+    clk = clocks.stop()
 
     # ---- end to end through the API with pinned host inputs
     e2e = run_e2e(args, api, cfg, steps_np, caches, ctx_all, ctx0, st, stream, dev)
@@ -441,6 +513,7 @@ def run_gpu(args):
             "kernels": kernels,
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "modes": modes,
             "gpu_launches": launches_per_step * K,
             "clocks": clk,
             "device_status": status,

@@ -14,7 +14,7 @@
  *   dfv_greedy_accept     per-node vocabulary argmax + greedy tree walk
  *   dfv_kv_commit         Q4_0 re-quantisation of the accepted K/V rows into
  *                         the cache; rejected rows are never written
- *   dfv_verify_step       the three above in one cooperative launch
+ *   dfv_verify_step       the three above in one launch
  *
  * plus dfv_kv_quantize_rows, the same Q4_0 quantiser used to fill a cache
  * from float rows (prefill).
@@ -92,6 +92,19 @@ typedef enum dfv_status {
  * and dequantised; F16: rounded to binary16, exact for bf16 values in
  * range), instead of their bf16 values. */
 #define DFV_KV_TREE_AS_CACHE 0x100
+/* Flag OR-ed into kv_format of dfv_verify_step and dfv_tree_verify_attn:
+ * launch the step so that it overlaps the previous kernel of the stream
+ * (programmatic dependent launch), the "pipelined" dependency mode in which
+ * only the KV dependency between consecutive steps is enforced. Before that
+ * kernel has completed, the step reads only q, tree_k, tree_v, parent,
+ * tokens and logits -- which that kernel must not write -- and its own
+ * workspace, and may OR bits into *status. ctx_len, the cache and every
+ * output are read and written only after it has completed, so a chain of
+ * steps over one cache gives the same results as plain launches.
+ * Consecutive pipelined calls in a stream must use different workspaces
+ * (two, used in turn, suffice). Needs one CTA on every SM: returns
+ * DFV_ERR_UNSUPPORTED on a device with more than 256 SMs. */
+#define DFV_STEP_PIPELINED 0x200
 
 #define DFV_DTYPE_F32 0
 #define DFV_DTYPE_BF16 1
@@ -124,6 +137,7 @@ int dfv_version(void);
  *   head_dim       D in {64, 128, 256}
  *   window         sliding window in positions, 0 = none
  *   kv_format      DFV_KV_Q4_0 or DFV_KV_F16, optionally | DFV_KV_TREE_AS_CACHE
+ *                  and | DFV_STEP_PIPELINED
  *   cache_capacity positions per head in the cache
  *   ctx_len        device int32[1], committed length C (read only)
  *   k_cache,v_cache  device cache in kv_format (layout above), read only
@@ -267,7 +281,9 @@ dfv_status dfv_kv_quantize_rows(int n_kv_heads, int head_dim, int kv_format, int
 
 /* ------------------------------------------------------------------------
  * dfv_verify_step -- one whole greedy tree-verify step (attention, argmax +
- * walk, commit) in ONE cooperative kernel launch on `stream`: one CTA per SM.
+ * walk, commit) in ONE kernel launch on `stream`: one CTA per SM, a
+ * cooperative launch (with DFV_STEP_PIPELINED: a programmatic dependent
+ * launch that overlaps the previous kernel, see the flag).
  * A split of the attention waits only for the other splits of its group
  * before merging, and the walker waits only until every CTA has read the
  * committed length and reported its argmax partials. Arguments and results
@@ -277,7 +293,7 @@ dfv_status dfv_kv_quantize_rows(int n_kv_heads, int head_dim, int kv_format, int
  * length. The workspace size covers either cache format.
  * `workspace` (dfv_verify_step_workspace_bytes) must be zeroed once before
  * its first use; each call leaves it ready for the next. Calls sharing a
- * workspace must not overlap on the GPU.
+ * workspace must not overlap on the GPU (two pipelined calls in a row would).
  * ---------------------------------------------------------------------- */
 size_t dfv_verify_step_workspace_bytes(int n_nodes, int n_q_heads, int n_kv_heads, int head_dim,
                                        int window, int cache_capacity, int vocab);

@@ -56,3 +56,33 @@ def test_host_side_rejections(lib):
     assert st == 2  # DFV_ERR_UNSUPPORTED (format)
     st = lib.dfv_kv_quantize_rows(4, 96, 2, 100, 0, 1, None, 0, 1, 1, None, None)
     assert st == 2
+
+
+def test_header_constants_match_binding():
+    """The binding's format codes, flags and status bits are the header's."""
+    from tree_verify_attention_gb300 import api
+    text = open(HEADER).read()
+    defs = {m.group(1): int(m.group(2), 0)
+            for m in re.finditer(r"#define\s+(DFV_\w+)\s+(0x[0-9a-fA-F]+|\d+)u?\b", text)}
+    assert defs["DFV_KV_F16"] == api.KV_F16
+    assert defs["DFV_KV_Q4_0"] == api.KV_Q4_0
+    assert defs["DFV_KV_TREE_AS_CACHE"] == api.KV_TREE_AS_CACHE
+    assert defs["DFV_STEP_PIPELINED"] == api.STEP_PIPELINED
+    assert defs["DFV_DTYPE_F32"] == api.DTYPE_F32 and defs["DFV_DTYPE_BF16"] == api.DTYPE_BF16
+    assert defs["DFV_MAX_NODES"] == api.MAX_NODES
+    for name in ("BAD_TREE", "DEPTH", "CAPACITY", "CTX", "BAD_PATH", "TIMEOUT"):
+        assert defs["DFV_DEV_" + name] == getattr(api, "DEV_" + name), name
+    # flags sit above the format byte and do not overlap
+    assert api.KV_TREE_AS_CACHE & 0xFF == 0 and api.STEP_PIPELINED & 0xFF == 0
+    assert api.KV_TREE_AS_CACHE & api.STEP_PIPELINED == 0
+
+
+def test_unknown_step_flag_rejected(lib):
+    # a flag bit the library does not know is refused before any device call
+    st = lib.dfv_verify_step(23, 16, 24, 4, 256, 2048, 2 | 0x400, 100, 1000, 1, None, None,
+                             None, None, None, None, None, None, None, 0.0, None, None, None,
+                             None, None, None, None, 0, None, None)
+    assert st == 2  # DFV_ERR_UNSUPPORTED
+    st = lib.dfv_tree_verify_attn(23, 16, 24, 4, 256, 2048, 2 | 0x800, 100, None, None, None,
+                                  None, None, None, None, 0.0, None, None, None, 0, None, None)
+    assert st == 2

@@ -14,6 +14,7 @@ DTYPE_BF16 = 1
 KV_F16 = 1
 KV_Q4_0 = 2
 KV_TREE_AS_CACHE = 0x100
+STEP_PIPELINED = 0x200
 _FORMATS = {"q4_0": KV_Q4_0, "f16": KV_F16}
 MAX_NODES = 65
 
@@ -163,7 +164,7 @@ def workspace(nbytes, device="cuda", stream=None):
 
 
 def tree_verify_attn(cache, q, tree_k, tree_v, parent, window, max_depth, out, lse, ws,
-                     scale=0.0, status=None, stream=None, tree_as_cache=False):
+                     scale=0.0, status=None, stream=None, tree_as_cache=False, pipelined=False):
     n, hq, d = q.shape
     hkv = tree_k.shape[1]
     _dev(q, "q", _BF16)
@@ -173,7 +174,8 @@ def tree_verify_attn(cache, q, tree_k, tree_v, parent, window, max_depth, out, l
     _dev(out, "out", _F32, n * hq * d)
     if lse is not None:
         _dev(lse, "lse", _F32, n * hq)
-    kvf = cache.kv_format | (KV_TREE_AS_CACHE if tree_as_cache else 0)
+    kvf = (cache.kv_format | (KV_TREE_AS_CACHE if tree_as_cache else 0)
+           | (STEP_PIPELINED if pipelined else 0))
     _check(lib().dfv_tree_verify_attn(
         n, max_depth, hq, hkv, d, window, kvf, cache.capacity, cache.ctx_len.data_ptr(),
         cache.k.data_ptr(), cache.v.data_ptr(), q.data_ptr(), tree_k.data_ptr(),
@@ -210,10 +212,14 @@ def kv_commit(cache, accept_len, path, tree_k, tree_v, status=None, stream=None)
 
 class VerifyStep:
     """Outputs and workspace of the verify step for one problem shape; call
-    :meth:`run` once per step. All buffers live on the device."""
+    :meth:`run` once per step. All buffers live on the device.
+
+    ``pipelined=True`` launches each step so that it overlaps the previous
+    kernel of the stream (``DFV_STEP_PIPELINED``); the object then keeps two
+    workspaces and uses them in turn, as consecutive pipelined steps need."""
 
     def __init__(self, n_nodes, n_q_heads, n_kv_heads, head_dim, window, capacity, vocab,
-                 max_depth=16, device="cuda"):
+                 max_depth=16, device="cuda", pipelined=False):
         self.shape = (n_nodes, n_q_heads, n_kv_heads, head_dim, window, capacity, vocab)
         self.max_depth = max_depth
         dev = torch.device(device)
@@ -228,7 +234,10 @@ class VerifyStep:
                                   vocab)
         if nb == 0:
             raise DfvError(f"unsupported step shape {self.shape}")
-        self.ws = workspace(nb, device=dev)
+        self.pipelined = bool(pipelined)
+        self.workspaces = [workspace(nb, device=dev) for _ in range(2 if self.pipelined else 1)]
+        self.ws = self.workspaces[0]
+        self._turn = 0
 
     def run(self, cache, q, tree_k, tree_v, parent, tokens, logits, scale=0.0, stream=None,
             tree_as_cache=False):
@@ -242,12 +251,15 @@ class VerifyStep:
         _dev(tokens, "tokens", _I32, n)
         _dev(logits, "logits", (torch.float32,) + _BF16, n * vocab)
         dt = DTYPE_F32 if logits.dtype == torch.float32 else DTYPE_BF16
-        kvf = cache.kv_format | (KV_TREE_AS_CACHE if tree_as_cache else 0)
+        kvf = (cache.kv_format | (KV_TREE_AS_CACHE if tree_as_cache else 0)
+               | (STEP_PIPELINED if self.pipelined else 0))
+        ws = self.workspaces[self._turn]
+        self._turn = (self._turn + 1) % len(self.workspaces)
         _check(lib().dfv_verify_step(
             n, self.max_depth, hq, hkv, d, window, kvf, cap, vocab, dt,
             cache.ctx_len.data_ptr(), cache.k.data_ptr(), cache.v.data_ptr(), q.data_ptr(),
             tree_k.data_ptr(), tree_v.data_ptr(), parent.data_ptr(), tokens.data_ptr(),
             logits.data_ptr(), float(scale), self.out.data_ptr(), self.lse.data_ptr(),
             self.argmax.data_ptr(), self.accept_len.data_ptr(), self.path.data_ptr(),
-            self.out_tokens.data_ptr(), self.ws.data_ptr(), self.ws.numel(),
+            self.out_tokens.data_ptr(), ws.data_ptr(), ws.numel(),
             self.status.data_ptr(), _stream(stream)), "dfv_verify_step")

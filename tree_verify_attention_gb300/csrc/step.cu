@@ -1,39 +1,44 @@
-// The whole greedy tree-verify step in one cooperative launch, with the
-// attention on the 5th-generation tensor cores (tcgen05, TMEM accumulators).
+// The whole greedy tree-verify step in one launch, with the attention on the
+// 5th-generation tensor cores (tcgen05, TMEM accumulators).
 //
 // "Luce DFlash: Qwen3.6-27B ..." (ai-navigate-news, ja), feature list: DDTree
 // tree-verify (block 16, budget 22), greedy verification, Q4_0 KV cache,
 // sliding-window flash attention at decode (window 2048). The step computes,
 // for the N = budget + 1 tree nodes, attention over the visible committed
 // keys and the node's ancestors, the argmax of every node's logits, the
-// greedy walk, and the Q4_0 commit of the accepted rows.
+// greedy walk, and the commit of the accepted rows in the cache format.
 //
-// One CTA per SM, one launch per step, two phases around one grid barrier.
-//
-// Phase A, per CTA. At t = 0 thread 0 starts 1-D bulk copies (TMA engine)
-// of everything the CTA reads from HBM: its logits slice, the bf16 Q rows
-// of its attention tile and its Q4_0 K/V chunk (128 keys x 144 bytes each
-// at D = 256), so their latencies overlap. Then:
-//   * the logits slice is scanned from shared memory into a (max, lowest
-//     index) partial;
-//   * tree K/V rows are quantised to Q4_0 into a staging area (on CTAs
-//     without an attention unit when there are any), so the commit after
-//     the walk is a plain copy;
-//   * attention unit = (KV head h, 128-row tile of the head's (node, query
-//     head) rows, range of 128-key chunks). Q -> fp16, K and V dequantised
-//     ((q - 8) * d, one rounding), all in 128-byte-swizzled smem with keys or
-//     rows as the outer index; S = Q K^T by tcgen05.mma into TMEM (M = 128
-//     rows, N = 128 keys, K = D); two threads per row read S from TMEM, mask
-//     (window, ancestors), exchange the row max, exp2, write P (fp16);
-//     O += P V by tcgen05.mma (M = 128, N = D, K = 128 keys; V as an
-//     MN-major operand). The running max only moves (O rescaled in TMEM)
-//     when a chunk's max exceeds it by more than 2^8, so P <= 256 fits fp16.
-//     The row's normalised O (fp16), max and sum go to the workspace.
-// Grid barrier (bounded wait; a timeout sets DFV_DEV_TIMEOUT).
-// Phase B: CTAs 1..G-1 merge the key splits of a slice of the output rows
-// by log-sum-exp; CTA 0 merges the argmax partials, walks the tree in one
-// warp, copies the pre-quantised accepted rows into the cache at C..C+L-1
-// and advances the committed length (every CTA read it before the barrier).
+// One CTA per SM, one launch per step, no grid-wide barrier. CTA roles:
+//   * attention units = (KV head h, 128-row tile of the head's (node, query
+//     head) rows, range of 128-key chunks); the tree chunk is processed
+//     first, by the last split of each (head, tile) group;
+//   * CTAs without a unit scan logits slices (the units of short row tiles
+//     take the rest); one of them is the walker.
+// At t = 0 thread 0 starts 1-D bulk copies (TMA engine) of the CTA's first
+// K / V chunk and its logits slices, and every thread loads its share of
+// the bf16 Q rows and tree rows, so that the latencies overlap. Then:
+//   * the logits slices are scanned from shared memory into (max, lowest
+//     index) partials; the tree rows are quantised into a staging area so
+//     that the commit after the walk is a plain copy;
+//   * per chunk: Q -> fp16, K and V decoded ((q - 8) * d, one rounding; or
+//     binary16 rows copied as they are) into 128-byte-swizzled smem;
+//     S = Q K^T by tcgen05.mma into TMEM (M = 128 rows, N = 128 keys,
+//     K = D); four threads per row read S from TMEM, mask (window,
+//     ancestors), exchange the row max, exp2, write P (fp16); O += P V by
+//     tcgen05.mma (M = 128, N = D, K = 128 keys; V as an MN-major
+//     operand). The running max only moves (O rescaled in TMEM) when a
+//     chunk's max exceeds it by more than 2^8, so P <= 256 fits fp16;
+//   * each split writes its normalised O (fp16), max and sum to the
+//     workspace and marks its ready word; the splits of a group wait for
+//     one another (bounded waits) and each merges a share of the group's
+//     rows by log-sum-exp;
+//   * the walker waits until every other CTA has read ctx and written its
+//     partials, merges the argmax partials, walks the tree in one warp,
+//     copies the staged accepted rows into the cache at C..C+L-1 and
+//     advances the committed length.
+// A pipelined launch (programmatic dependent launch) does everything that
+// reads only the step's own inputs -- the logits scan, Q, the tree -- while
+// the previous kernel of the stream finishes, and waits for it before ctx.
 
 #include <math.h>
 
@@ -68,6 +73,7 @@ struct StepParams {
   uint32_t group_m;  // ceil(2^32 / group) (0 when group == 1): row -> node by multiply-high
   int do_accept;
   int tree_q;        // attend Q4_0-quantised-and-dequantised tree rows
+  int pipelined;     // launched to overlap the previous kernel of the stream
   int walker;        // CTA that merges the argmax partials, walks and commits
   int walker_local;  // 1: it quantises the tree rows into its own smem
   float scale_log2;
@@ -513,8 +519,13 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
   __shared__ int s_wpar[kMaxNodes], s_wtok[kMaxNodes];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int G = gridDim.x, blk = blockIdx.x;
+  const int G = gridDim.x;
+  // A pipelined step hands the roles out in reverse, so that the CTAs that
+  // start first, on the SMs the previous step frees first, are the walker
+  // and the logits CTAs: their work does not wait for that step.
+  const int blk = p.pipelined ? G - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
   const int N = p.n_nodes;
+  grid_dep_launch_dependents();   // the next step may start on SMs this one frees
 
   // ---- this CTA's attention unit
   const int unit = blk < p.units ? blk : -1;
@@ -632,14 +643,10 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       }
     }
   }
-  // Thread 0 first: barriers, the logits copies, the read of ctx, the first
-  // K / V copy -- ahead of its own loads below (the barrier-init fence would
-  // wait for them).
-  if (tid == 0) {
-    mbar_init(bar_kv, 1);
-    mbar_init(bar_mma, 1);
-    mbar_init(bar_lg, 1);
-    fence_mbar_init();
+  // Thread 0: the read of ctx, the split group's arrival and the first K / V
+  // copy. Everything a step reads or writes that the previous step may
+  // write (ctx, the cache, the outputs) comes after this.
+  auto ctx_and_first_kv = [&]() {
     C = static_cast<int>(ld_acquire_gpu(reinterpret_cast<const unsigned int*>(p.ctx_len)));
     // the group arrival's old value is only needed at the end of the unit
     if (unit >= 0 && p.splits > 1) arrive_old = atomicAdd(p.bar + 4 + 2 * (unit / p.splits), 1u);
@@ -652,6 +659,16 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     if constexpr (L::kBulk && kQ4) {
       if (first_kv) issue_kv(c0);
     }
+  };
+  // Thread 0 first: barriers, the read of ctx and the first K / V copy (not
+  // yet when pipelined), the logits copies -- ahead of its own loads below
+  // (the barrier-init fence would wait for them).
+  if (tid == 0) {
+    mbar_init(bar_kv, 1);
+    mbar_init(bar_mma, 1);
+    mbar_init(bar_lg, 1);
+    fence_mbar_init();
+    if (!p.pipelined) ctx_and_first_kv();
     // the logits copies go after the K/V copy, which is on the critical path
     if (lreg) {
       uint32_t total = 0;
@@ -673,7 +690,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       }
     }
     // nothing for the walker to wait for but the read of ctx above
-    if (p.do_accept && blk != p.walker && !late_signal) atomicAdd(p.bar + 2, 1u);
+    if (!p.pipelined && p.do_accept && blk != p.walker && !late_signal) atomicAdd(p.bar + 2, 1u);
   }
   if (unit >= 0 && warp == 2) {
     tc::tmem_alloc(s_tmem, kTmemCols);
@@ -742,13 +759,13 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     }
   }
   __syncthreads();   // barriers initialised, tree bookkeeping done, ctx known
-  C = s_C;
-  derive();
+                     // (unless pipelined)
 
-  // ---- logits: CTAs without an attention unit scan their slice now; slices
-  // beyond one per CTA (or unaligned rows) go through plain loads
-  if (p.do_accept) {
-    if (unit < 0 && lreg) scan_slices<LT>(p, lstage, ls0, lsn, bar_lg, &s_ok);
+  // ---- logits: CTAs without an attention unit scan their slices now (and
+  // so do the units when pipelined); slices beyond one per CTA (or unaligned
+  // rows) go through plain loads
+  auto accept_inputs = [&](bool units_too) {
+    if (lreg && (unit < 0 || units_too)) scan_slices<LT>(p, lstage, ls0, lsn, bar_lg, &s_ok);
     if (!p.lbulk) plain_slices<LT>(p, blk, G);
     // ---- the walker keeps the tree's parents and tokens in smem
     if (blk == p.walker && tid < N) {
@@ -767,6 +784,23 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       prequant_tree<D, FMT>(p, qdst, static_cast<int>(static_cast<long>(bq) * tot / nq),
                        static_cast<int>(static_cast<long>(bq + 1) * tot / nq));
     }
+  };
+  if (!p.pipelined) {
+    C = s_C;
+    derive();
+  }
+  // pipelined: this reads only the step's own inputs and workspace, and runs
+  // while the previous kernel finishes; ctx and the K / V copy come after it
+  if (p.do_accept) accept_inputs(p.pipelined != 0);
+  if (p.pipelined) {
+    grid_dep_wait();
+    if (tid == 0) {
+      ctx_and_first_kv();
+      if (p.do_accept && blk != p.walker && !late_signal) atomicAdd(p.bar + 2, 1u);
+    }
+    __syncthreads();
+    C = s_C;
+    derive();
   }
 
   if (unit < 0 && late_signal) {
@@ -787,7 +821,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         s_row_lo[tid] = 0x7fffffff;
       }
     }
-    if (lreg) scan_slices<LT>(p, lstage, ls0, lsn, bar_lg, &s_ok);   // the staged logits slices first
+    if (lreg && !p.pipelined) scan_slices<LT>(p, lstage, ls0, lsn, bar_lg, &s_ok);   // the staged logits slices first
     else if (late_signal) __syncthreads();   // every thread's tree rows written
     if (late_signal) signal_done();
     tc::fence_after_sync();
@@ -1418,6 +1452,14 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
   return true;
 }
 
+// A plain step is a cooperative launch (all CTAs resident at once). A
+// pipelined one is launched with programmatic stream serialisation instead:
+// its CTAs start on the SMs the previous kernel frees and wait in the kernel
+// (griddepcontrol.wait) before touching ctx, the cache or the outputs. Its
+// CTAs still all become resident, as the previous kernel never waits on
+// them; and as each CTA takes a whole SM (one per SM: the register file),
+// the step after it can only start once the one before it has completed,
+// which is why two workspaces, used in turn, suffice.
 template <int D, typename LT, int FMT>
 static dfv_status step_launch_dt(StepParams& p, const StepPlan& pl, cudaStream_t stream) {
   static int configured[64] = {};
@@ -1427,10 +1469,11 @@ static dfv_status step_launch_dt(StepParams& p, const StepPlan& pl, cudaStream_t
     if (cudaFuncSetAttribute(step_kernel<D, LT, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              StepSmem<D>::kBytes) != cudaSuccess)
       return DFV_ERR_CUDA;
+    // exactly one CTA per SM: each holds all of the SM's TMEM columns
     int nb = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, step_kernel<D, LT, FMT>, kStepThreads,
                                                       StepSmem<D>::kBytes) != cudaSuccess ||
-        nb < 1)
+        nb != 1)
       return DFV_ERR_CUDA;
     configured[dev] = 1;
   }
@@ -1440,8 +1483,13 @@ static dfv_status step_launch_dt(StepParams& p, const StepPlan& pl, cudaStream_t
   cfg.dynamicSmemBytes = StepSmem<D>::kBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  if (p.pipelined) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, step_kernel<D, LT, FMT>, p) == cudaSuccess ? DFV_OK : DFV_ERR_CUDA;
@@ -1483,7 +1531,8 @@ dfv_status step_launch(bool with_accept, int n_nodes, int max_depth, int hq, int
                        int32_t* path, int32_t* out_tokens, void* workspace, size_t ws_bytes,
                        uint32_t* status, cudaStream_t stream) {
   const int fmt = kv_format & 0xFF, flags = kv_format & ~0xFF;
-  if ((fmt != DFV_KV_Q4_0 && fmt != DFV_KV_F16) || (flags & ~DFV_KV_TREE_AS_CACHE) != 0)
+  if ((fmt != DFV_KV_Q4_0 && fmt != DFV_KV_F16) ||
+      (flags & ~(DFV_KV_TREE_AS_CACHE | DFV_STEP_PIPELINED)) != 0)
     return DFV_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128 && head_dim != 256) return DFV_ERR_UNSUPPORTED;
   if (with_accept && logits_dtype != DFV_DTYPE_F32 && logits_dtype != DFV_DTYPE_BF16)
@@ -1501,6 +1550,8 @@ dfv_status step_launch(bool with_accept, int n_nodes, int max_depth, int hq, int
       (with_accept && !aligned(logits, 16)))
     return DFV_ERR_INVALID;
   if (ws_bytes < pl.ws_total) return DFV_ERR_WORKSPACE;
+  // pipelined: one CTA on every SM (see step_launch_dt)
+  if ((flags & DFV_STEP_PIPELINED) && pl.grid != sm_count()) return DFV_ERR_UNSUPPORTED;
   StepParams p;
   p.n_nodes = n_nodes;
   p.max_depth = max_depth;
@@ -1525,6 +1576,7 @@ dfv_status step_launch(bool with_accept, int n_nodes, int max_depth, int hq, int
   // binary16 tree rows are exact in the cache format, so the flag only
   // changes anything for Q4_0
   p.tree_q = (flags & DFV_KV_TREE_AS_CACHE) && fmt == DFV_KV_Q4_0 ? 1 : 0;
+  p.pipelined = (flags & DFV_STEP_PIPELINED) ? 1 : 0;
   p.walker = pl.walker;
   p.walker_local = pl.walker_local;
   for (int i = 0; i < kMaxStepGrid; ++i) p.lslot[i] = pl.lslot[i];
