@@ -316,6 +316,31 @@ int dfv_verify_step_launches(int n_nodes, int n_q_heads, int n_kv_heads, int hea
 /* Zero `bytes` of a caller-owned workspace on `stream` (no allocation). */
 dfv_status dfv_workspace_clear(void* workspace, size_t bytes, dfv_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * dfv_build_tree_mask -- depth and ancestor-or-self bitmask of every node
+ * of a draft tree: the tree half of the visibility rule above ("Luce
+ * DFlash ..." feature list: DDTree tree-verify, where a node attends to its
+ * ancestors and itself). The attention computes the same values inside its
+ * kernel; this helper is for callers that build their own masks.
+ *
+ *   n_nodes    N, 1..DFV_MAX_NODES
+ *   parent     device int32 [N]; parent[0] is ignored (the root); an entry
+ *              outside [0, i) is treated as 0 and sets DFV_DEV_BAD_TREE
+ *   depth      device int32 [N], written: depth[0] = 0,
+ *              depth[i] = depth[parent[i]] + 1
+ *   anc_mask   device uint32 [N][DFV_MASK_WORDS], written: bit (t % 32) of
+ *              word t / 32 of row i is set iff node t is i or an ancestor
+ *              of i; bits of nodes >= N are zero
+ *   status     device uint32[1] (DFV_DEV_* bits OR-ed in), may be NULL
+ *
+ * One launch of one CTA on `stream`. Returns DFV_ERR_INVALID for a bad
+ * n_nodes or a NULL parent / depth / anc_mask, DFV_ERR_CUDA if the launch
+ * fails; nothing is written then.
+ * ---------------------------------------------------------------------- */
+#define DFV_MASK_WORDS ((DFV_MAX_NODES + 31) / 32) /* 3 */
+dfv_status dfv_build_tree_mask(int n_nodes, const int32_t* parent, int32_t* depth,
+                               uint32_t* anc_mask, uint32_t* status, dfv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

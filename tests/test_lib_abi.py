@@ -86,3 +86,10 @@ def test_unknown_step_flag_rejected(lib):
     st = lib.dfv_tree_verify_attn(23, 16, 24, 4, 256, 2048, 2 | 0x800, 100, None, None, None,
                                   None, None, None, None, 0.0, None, None, None, 0, None, None)
     assert st == 2
+
+
+def test_tree_mask_host_rejections(lib):
+    # bad node counts and missing buffers are refused before any launch
+    for n in (0, 66, -1):
+        assert lib.dfv_build_tree_mask(n, None, None, None, None, None) == 1
+    assert lib.dfv_build_tree_mask(5, None, None, None, None, None) == 1

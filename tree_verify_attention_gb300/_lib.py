@@ -27,6 +27,7 @@ SIGNATURES = {
     "dfv_verify_step": (_i32, [_i32] * 10 + [_vp] * 9 + [_f32] + [_vp] * 6 + [_vp, _sz, _vp, _vp]),
     "dfv_verify_step_launches": (_i32, [_i32] * 6),
     "dfv_workspace_clear": (_i32, [_vp, _sz, _vp]),
+    "dfv_build_tree_mask": (_i32, [_i32] + [_vp] * 5),
 }
 
 _lib = None

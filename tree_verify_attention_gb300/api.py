@@ -17,6 +17,7 @@ KV_TREE_AS_CACHE = 0x100
 STEP_PIPELINED = 0x200
 _FORMATS = {"q4_0": KV_Q4_0, "f16": KV_F16}
 MAX_NODES = 65
+MASK_WORDS = (MAX_NODES + 31) // 32
 
 DEV_BAD_TREE = 0x1
 DEV_DEPTH = 0x2
@@ -181,6 +182,17 @@ def tree_verify_attn(cache, q, tree_k, tree_v, parent, window, max_depth, out, l
         cache.k.data_ptr(), cache.v.data_ptr(), q.data_ptr(), tree_k.data_ptr(),
         tree_v.data_ptr(), parent.data_ptr(), float(scale), out.data_ptr(), _p(lse),
         ws.data_ptr(), ws.numel(), _p(status), _stream(stream)), "dfv_tree_verify_attn")
+
+
+def build_tree_mask(parent, depth, anc_mask, status=None, stream=None):
+    """depth [N] (int32) and ancestor-or-self bitmasks [N, MASK_WORDS]
+    (int32 tensor holding the uint32 words) of the tree given by ``parent``."""
+    n = parent.numel()
+    _dev(parent, "parent", _I32, n)
+    _dev(depth, "depth", _I32, n)
+    _dev(anc_mask, "anc_mask", _I32, n * MASK_WORDS)
+    _check(lib().dfv_build_tree_mask(n, parent.data_ptr(), depth.data_ptr(), anc_mask.data_ptr(),
+                                     _p(status), _stream(stream)), "dfv_build_tree_mask")
 
 
 def greedy_accept(logits, parent, tokens, argmax, accept_len, path, out_tokens, ws,

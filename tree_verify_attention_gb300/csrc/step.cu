@@ -832,6 +832,10 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int r = (warp & 3) * 32 + lane;   // this thread's row
     const int hc = warp >> 2;               // its quarter of the keys / of O's columns
+    // A warp whose 32 rows all lie past the last row (the short tile) skips
+    // the second half of the softmax and the epilogue: its P rows keep the
+    // finite operand values under them, and its O rows reach no output.
+    auto rows_live = [&]() { return mt * kRowsPerTile + (warp & 3) * 32 < p.rows; };
     uint32_t ph_kv = 0, ph_mma = 0;
     float m_run = -INFINITY, l_half = 0.f;
     bool o_valid = false, alive = true;
@@ -1026,6 +1030,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         }
         s_pmax[hc][r] = fmaxf(fmaxf(cm[0], cm[1]), fmaxf(cm[2], cm[3]));
         __syncthreads();
+        if (rows_live()) {
         const float cmax = fmaxf(fmaxf(s_pmax[0][r], s_pmax[1][r]), fmaxf(s_pmax[2][r], s_pmax[3][r]));
         float alpha = 1.f;
         bool rescale = false;
@@ -1066,6 +1071,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
             if constexpr (CW == 32) tc::st32(t_o + lane_base + col, ov);
             else tc::st16(t_o + lane_base + col, ov);
           }
+        }
         }
       }
       fence_proxy_async_smem();
@@ -1118,7 +1124,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         inv[i] = l > 0.f ? __fdividef(1.f, l) : 0.f;
       }
 #pragma unroll 1
-      for (int c = 0; c < (D / 4) / CW; ++c) {
+      for (int c = 0; c < (rows_live() ? (D / 4) / CW : 0); ++c) {
         const int col = hc * (D / 4) + c * CW;
         float ov[32];
         if constexpr (CW == 32) tc::ld32(t_o + lane_base + col, ov);
