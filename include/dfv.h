@@ -81,7 +81,8 @@ typedef enum dfv_status {
 #define DFV_DEV_BAD_TREE 0x1u  /* parent[i] outside [0, i): treated as 0      */
 #define DFV_DEV_DEPTH 0x2u     /* a node deeper than max_depth (still run)    */
 #define DFV_DEV_CAPACITY 0x4u  /* ctx_len + accept_len > capacity: no write   */
-#define DFV_DEV_CTX 0x8u       /* *ctx_len outside [0, capacity]: no work     */
+#define DFV_DEV_CTX 0x8u       /* *ctx_len outside [0, capacity]: nothing    */
+                               /* committed; attention uses it clamped       */
 #define DFV_DEV_BAD_PATH 0x10u /* path entry outside [0, n_nodes): no write   */
 #define DFV_DEV_TIMEOUT 0x20u  /* a bounded wait gave up; outputs undefined   */
 

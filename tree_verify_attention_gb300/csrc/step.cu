@@ -380,8 +380,8 @@ __device__ __noinline__ void prequant_tree(const StepParams& p, uint8_t* qdst, i
 // owes (argmax partials, tree rows), merges the argmax partials per node,
 // walks the tree from the root and commits the accepted rows to the cache.
 template <int D, int FMT>
-__device__ __noinline__ void walker_tail(const StepParams& p, int G, int C, uint8_t* sQ, const uint8_t* sK,
-                                         const int* s_wpar, const int* s_wtok) {
+__device__ __noinline__ void walker_tail(const StepParams& p, int G, int C, bool ctx_ok, uint8_t* sQ,
+                                         const uint8_t* sK, const int* s_wpar, const int* s_wtok) {
   using L = StepSmem<D>;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int N = p.n_nodes;
@@ -471,7 +471,10 @@ __device__ __noinline__ void walker_tail(const StepParams& p, int G, int C, uint
   }
   __syncthreads();
   const int Lc = s_L, Cc = C;
-  if (Cc + Lc > p.capacity) {
+  if (!ctx_ok) {
+    // the committed length was outside [0, capacity] (reported at entry):
+    // nothing is committed
+  } else if (Cc + Lc > p.capacity) {
     if (tid == 0) report(p.status, DFV_DEV_CAPACITY);
   } else {
     constexpr int kCRowB = kv_row_bytes(FMT, D);   // bytes of one cache row
@@ -540,6 +543,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
   // that its report to the walker below cannot overtake it) and shared
   // through smem after the first barrier
   __shared__ int s_C;
+  __shared__ int s_ctx_ok;     // ctx was inside [0, capacity]
   __shared__ uint32_t s_tag;   // this launch's ready tag of the unit's group
   // Chunks [c0, c1) of the unit; the tree chunk (N <= 65 keys: one chunk,
   // the last, held by the last split) is processed first, then the
@@ -650,9 +654,11 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     C = static_cast<int>(ld_acquire_gpu(reinterpret_cast<const unsigned int*>(p.ctx_len)));
     // the group arrival's old value is only needed at the end of the unit
     if (unit >= 0 && p.splits > 1) arrive_old = atomicAdd(p.bar + 4 + 2 * (unit / p.splits), 1u);
+    s_ctx_ok = 1;
     if (C < 0 || C > p.capacity) {
       if (blk == 0) report(p.status, DFV_DEV_CTX);
       C = C < 0 ? 0 : p.capacity;
+      s_ctx_ok = 0;
     }
     s_C = C;
     derive();
@@ -1195,7 +1201,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
   // ---- the walker: once every other CTA has read ctx and written its
   // argmax partial, merge the partials, walk and commit -- all before the
   // group barriers, under the attention of the other CTAs
-  if (p.do_accept && blk == p.walker) walker_tail<D, FMT>(p, G, C, sQ, sK, s_wpar, s_wtok);
+  if (p.do_accept && blk == p.walker) walker_tail<D, FMT>(p, G, C, s_ctx_ok != 0, sQ, sK, s_wpar, s_wtok);
 
   // ================================================================ merge
   // Each of the `splits` CTAs of a (KV head, row tile) group waits for the
