@@ -525,16 +525,21 @@ def run_gpu(args):
 
 
 def kernel_source_hash():
-    """Hash of the CUDA sources, to tell whether recorded ncu counters still
-    describe the kernel being timed."""
+    """Hash of the CUDA sources with comments and whitespace removed, to tell
+    whether recorded ncu counters still describe the kernel being timed (an
+    edit of comments alone keeps the hash)."""
     import hashlib
+    import re
     d = os.path.join(ROOT, "tree_verify_attention_gb300", "csrc")
     h = hashlib.sha256()
     for f in sorted(os.listdir(d)):
         if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(d, f), encoding="utf-8") as fh:
+                text = fh.read()
+            text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+            text = re.sub(r"//[^\n]*", " ", text)
             h.update(f.encode())
-            with open(os.path.join(d, f), "rb") as fh:
-                h.update(fh.read())
+            h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -628,8 +628,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     }
   }
   // Q: this thread's 16-byte pieces of the tile's bf16 rows, converted into
-  // the fp16 swizzled tile (sQ) once they have landed; rows past the last
-  // are zero
+  // the fp16 swizzled tile (sQ) before the first barrier; rows past the
+  // last are zero
   constexpr int QU = kRowsPerTile * (D / 8) / kStepThreads;
   static_assert(QU >= 1, "Q pieces per thread");
   uint4 qv[QU];
@@ -666,9 +666,11 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       if (first_kv) issue_kv(c0);
     }
   };
-  // Thread 0 first: barriers, the read of ctx and the first K / V copy (not
-  // yet when pipelined), the logits copies -- ahead of its own loads below
-  // (the barrier-init fence would wait for them).
+  // Thread 0, once every thread's Q and tree loads are in flight: barriers,
+  // the read of ctx and the first K / V copy (not yet when pipelined), the
+  // logits copies. (Its barrier-init fence waits for its own loads above;
+  // issuing the copies before any load was measured slower, since the
+  // first barrier then waits longer for warp 0's Q pieces.)
   if (tid == 0) {
     mbar_init(bar_kv, 1);
     mbar_init(bar_mma, 1);
