@@ -48,6 +48,7 @@ def parse_args(argv=None):
     ap.add_argument("--pool", type=int, default=POOL, help="distinct step inputs")
     ap.add_argument("--replicas", type=int, default=REPLICAS, help="KV-cache replicas")
     ap.add_argument("--cpu-child", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-start-at", type=float, default=0.0, help=argparse.SUPPRESS)
     ap.add_argument("--source-hash", action="store_true", help="print the kernel source hash")
     ap.add_argument("--fmt", choices=["q4_0", "f16"], default="q4_0",
                     help="KV-cache format (the headline workload is Q4_0)")
@@ -146,9 +147,11 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- CPU oracle timing
 
-def cpu_oracle_child(seconds, max_steps):
+def cpu_oracle_child(seconds, max_steps, start_at=0.0):
     """Time the oracle's whole verify step on a bounded sample of the
-    workload (runs in a single-threaded child process)."""
+    workload (runs in a single-threaded child process). With ``start_at``
+    (a wall-clock time) the timed loop starts then and runs for ``seconds``,
+    so that concurrent children overlap."""
     import numpy as np
     import oracle
     from tree_verify_attention_gb300 import workload as W
@@ -163,6 +166,8 @@ def cpu_oracle_child(seconds, max_steps):
     inputs = [W.make_step(cfg, i) for i in range(4)]
     ctx = cfg.ctx_len
     n = 0
+    if start_at > 0:
+        time.sleep(max(0.0, start_at - time.time()))
     t0 = time.perf_counter()
     while True:
         s = inputs[n % len(inputs)]
@@ -174,7 +179,37 @@ def cpu_oracle_child(seconds, max_steps):
         el = time.perf_counter() - t0
         if n >= max_steps or (el >= seconds and n >= 2):
             break
-    print(json.dumps({"steps": n, "seconds": el, "value": n / el}))
+    print(json.dumps({"steps": n, "seconds": el, "value": n / el,
+                      "late": int(start_at > 0 and time.time() - el > start_at + 1.0)}))
+
+
+def run_cpu_oracle_all_cores(seconds, max_procs=32):
+    """The same oracle on every host core at once: one single-threaded child
+    per core, each on its own sequence, timed loops aligned to one start
+    time; the value is the sum of the children's steps/s."""
+    cores = min(len(os.sched_getaffinity(0)), max_procs)
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    start_at = time.time() + 30.0            # after every child's setup
+    procs = [subprocess.Popen([sys.executable, os.path.abspath(__file__), "--cpu-child",
+                               "--cpu-seconds", str(seconds), "--cpu-start-at", str(start_at)],
+                              env=env, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
+             for _ in range(cores)]
+    rates, steps, late = [], 0, 0
+    for pr in procs:
+        out, err = pr.communicate()
+        if pr.returncode != 0:
+            raise RuntimeError("CPU oracle timing failed:\n" + err[-2000:])
+        res = json.loads(out.strip().splitlines()[-1])
+        rates.append(res["value"])
+        steps += res["steps"]
+        late += int(res.get("late", 0))
+    return {"value": sum(rates), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"{cores} single-threaded oracle processes, one sequence each "
+                       f"(verify_step at ctx 61440), timed loops of {seconds:.0f} s started "
+                       f"together ({late} started late): {steps} steps in all")}
 
 
 def run_cpu_oracle(seconds, max_steps=10 ** 9):
@@ -484,7 +519,7 @@ def run_gpu(args):
             "algorithmic_bytes": kv_b + lg_b,
             "tensor_tflops": flops / t_launch / 1e12, "tensor_peak": tf}
 
-    cpu = None
+    cpu = cpu_all = None
     if rank == 0 and not args.no_cpu_baseline:
         try:
             r = run_cpu_oracle(args.cpu_seconds)
@@ -493,6 +528,11 @@ def run_gpu(args):
         except Exception as ex:  # reported, not fatal
             cpu = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
                    "sample": f"failed: {ex}"[:300]}
+        try:
+            cpu_all = run_cpu_oracle_all_cores(args.cpu_seconds)
+        except Exception as ex:  # reported, not fatal
+            cpu_all = {"value": None, "unit": UNIT, "cores": None, "kind": "oracle",
+                       "sample": f"failed: {ex}"[:300]}
 
     if rank == 0:
         line = {
@@ -512,6 +552,7 @@ def run_gpu(args):
             "roofline": roof,
             "kernels": kernels,
             "cpu_baseline": cpu,
+            "cpu_baseline_all_cores": cpu_all,
             "e2e": e2e,
             "modes": modes,
             "gpu_launches": launches_per_step * K,
@@ -767,7 +808,8 @@ def main(argv=None):
         print(kernel_source_hash())
         return
     if args.cpu_child:
-        cpu_oracle_child(args.cpu_seconds, args.steps)
+        cpu_oracle_child(args.cpu_seconds, args.steps if not args.cpu_start_at else 10 ** 9,
+                         args.cpu_start_at)
         return
     if args.impl == "reference":
         run_reference(args)
