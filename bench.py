@@ -513,7 +513,8 @@ def run_gpu(args):
     }
     roof = {"kernel": "step_kernel<256>", "bound": "hbm",
             "achieved": (kv_b + lg_b) / t_launch / 1e9, "peak": hbm, "unit": "GB/s",
-            "frac": (kv_b + lg_b) / t_launch / 1e9 / hbm, "traffic": recorded_traffic(),
+            "frac": (kv_b + lg_b) / t_launch / 1e9 / hbm,
+            "traffic": recorded_traffic(args.fmt, args.tree_as_cache),
             "peak_source": peak_src + " copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
             "duration": "CUDA events over the timed graph region / launches",
             "algorithmic_bytes": kv_b + lg_b,
@@ -584,9 +585,12 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
+def recorded_traffic(fmt="q4_0", tree_as_cache=False):
     """DRAM bytes per step-kernel launch from the committed ncu summary, or
-    None when the kernel sources changed since it was taken."""
+    None when the kernel sources changed since it was taken or the run is
+    not the one it was taken on (the Q4_0 cache, tree rows as given)."""
+    if fmt != "q4_0" or tree_as_cache:
+        return None
     rec = {}
     try:
         with open(os.path.join(ROOT, "profiles", "step_kernel_traffic.txt")) as f:
