@@ -65,7 +65,7 @@ def _assert_same(a, b, what):
 
 @pytest.mark.parametrize("fmt,tree_as_cache", [("q4_0", False), ("f16", False), ("q4_0", True)],
                          ids=["q4_0", "f16", "q4_0-tree-as-cache"])
-@pytest.mark.parametrize("cfg", [W.SHORT, W.LONG_WINDOW], ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", [W.TINY, W.SHORT, W.LONG_WINDOW], ids=lambda c: c.name)
 def test_pipelined_chain_equals_plain(cfg, fmt, tree_as_cache):
     """Every step's outputs, the committed length and every cache byte are
     bit-identical between the pipelined and the plain chain (the kernel's
