@@ -147,7 +147,7 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- CPU oracle timing
 
-def cpu_oracle_child(seconds, max_steps, start_at=0.0):
+def cpu_oracle_child(seconds, max_steps, start_at=0.0, warmup=0):
     """Time the oracle's whole verify step on a bounded sample of the
     workload (runs in a single-threaded child process). With ``start_at``
     (a wall-clock time) the timed loop starts then and runs for ``seconds``,
@@ -165,21 +165,27 @@ def cpu_oracle_child(seconds, max_steps, start_at=0.0):
     del kf, vf
     inputs = [W.make_step(cfg, i) for i in range(4)]
     ctx = cfg.ctx_len
+
+    def one(k, ctx):
+        s = inputs[k % len(inputs)]
+        return oracle.step.verify_step(kc, vc, ctx, cfg.window, W.bf16_bits_to_f32(s.q),
+                                       W.bf16_bits_to_f32(s.k_tree), W.bf16_bits_to_f32(s.v_tree),
+                                       s.parent, s.tokens,
+                                       W.bf16_bits_to_f32(s.logits))["ctx_len"]
+
+    for k in range(warmup):                 # untimed
+        ctx = one(k, ctx)
     n = 0
     if start_at > 0:
         time.sleep(max(0.0, start_at - time.time()))
     t0 = time.perf_counter()
     while True:
-        s = inputs[n % len(inputs)]
-        res = oracle.step.verify_step(kc, vc, ctx, cfg.window, W.bf16_bits_to_f32(s.q),
-                                      W.bf16_bits_to_f32(s.k_tree), W.bf16_bits_to_f32(s.v_tree),
-                                      s.parent, s.tokens, W.bf16_bits_to_f32(s.logits))
-        ctx = res["ctx_len"]
+        ctx = one(warmup + n, ctx)
         n += 1
         el = time.perf_counter() - t0
         if n >= max_steps or (el >= seconds and n >= 2):
             break
-    print(json.dumps({"steps": n, "seconds": el, "value": n / el,
+    print(json.dumps({"steps": n, "seconds": el, "value": n / el, "warmup": warmup,
                       "late": int(start_at > 0 and time.time() - el > start_at + 1.0)}))
 
 
@@ -212,20 +218,22 @@ def run_cpu_oracle_all_cores(seconds, max_procs=32):
                        f"together ({late} started late): {steps} steps in all")}
 
 
-def run_cpu_oracle(seconds, max_steps=10 ** 9):
+def run_cpu_oracle(seconds, max_steps=10 ** 9, warmup=0):
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = "1"
     env["CUDA_VISIBLE_DEVICES"] = ""
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-child",
-                        "--cpu-seconds", str(seconds), "--steps", str(max_steps)],
+                        "--cpu-seconds", str(seconds), "--steps", str(max_steps),
+                        "--warmup", str(warmup)],
                        env=env, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("CPU oracle timing failed:\n" + r.stderr[-2000:])
     res = json.loads(r.stdout.strip().splitlines()[-1])
     res["sample"] = (f"oracle verify_step (fp64 tree attention over the 2047-key window, "
                      f"23 x 151936 argmax, greedy walk, Q4_0 commit) at ctx 61440: "
-                     f"{res['steps']} consecutive steps, {res['seconds']:.1f} s, one thread")
+                     f"{res['steps']} consecutive steps after {res['warmup']} untimed ones, "
+                     f"{res['seconds']:.1f} s, one thread")
     return res
 
 
@@ -235,11 +243,12 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    res = run_cpu_oracle(seconds=min(60.0, args.cpu_seconds * 4), max_steps=args.steps)
+    res = run_cpu_oracle(seconds=min(60.0, args.cpu_seconds * 4), max_steps=args.steps,
+                         warmup=min(10, max(3, args.warmup)))
     cpu = {"value": res["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
            "sample": res["sample"]}
     line = {"impl": "reference", "metric": METRIC, "value": res["value"], "unit": UNIT,
-            "n_gpus": args.gpus, "steps": res["steps"], "warmup": 0,
+            "n_gpus": args.gpus, "steps": res["steps"], "warmup": res["warmup"],
             "ms_per_step": 1000.0 * res["seconds"] / res["steps"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "ctx": 61440, "window": 2048, "budget": 22,
@@ -523,7 +532,7 @@ def run_gpu(args):
     cpu = cpu_all = None
     if rank == 0 and not args.no_cpu_baseline:
         try:
-            r = run_cpu_oracle(args.cpu_seconds)
+            r = run_cpu_oracle(args.cpu_seconds, warmup=3)
             cpu = {"value": r["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
                    "sample": r["sample"]}
         except Exception as ex:  # reported, not fatal
@@ -813,7 +822,7 @@ def main(argv=None):
         return
     if args.cpu_child:
         cpu_oracle_child(args.cpu_seconds, args.steps if not args.cpu_start_at else 10 ** 9,
-                         args.cpu_start_at)
+                         args.cpu_start_at, args.warmup if not args.cpu_start_at else 0)
         return
     if args.impl == "reference":
         run_reference(args)
