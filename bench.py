@@ -49,6 +49,8 @@ def parse_args(argv=None):
     ap.add_argument("--replicas", type=int, default=REPLICAS, help="KV-cache replicas")
     ap.add_argument("--cpu-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--cpu-start-at", type=float, default=0.0, help=argparse.SUPPRESS)
+    ap.add_argument("--clock-log", default=None,
+                    help="also write the raw nvidia-smi clock samples to this CSV file")
     ap.add_argument("--source-hash", action="store_true", help="print the kernel source hash")
     ap.add_argument("--fmt", choices=["q4_0", "f16"], default="q4_0",
                     help="KV-cache format (the headline workload is Q4_0)")
@@ -444,8 +446,11 @@ def run_gpu(args):
         gpu_id = u if u.startswith("GPU-") else "GPU-" + u
     except Exception:
         gpu_id = None
-    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-    clocks = ClockSampler(gpu_id, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv"))
+    log = None
+    if args.clock_log:
+        log = f"{args.clock_log}.rank{rank}.csv" if world > 1 else args.clock_log
+        os.makedirs(os.path.dirname(os.path.abspath(log)), exist_ok=True)
+    clocks = ClockSampler(gpu_id, log)
     clocks.start()
 
     # ---- warm-up: W steps, repeated for about a second so clocks settle
