@@ -110,6 +110,41 @@ def pin_commit_positions(CM, Q):
     assert np.array_equal(kc[:, :C], k0[:, :C]) and np.array_equal(kc[:, C + 3:], k0[:, C + 3:])
 
 
+def pin_f16_golden(F):
+    with open(os.path.join(os.path.dirname(__file__), "golden", "f16_worked_examples.json")) as f:
+        for ex in json.load(f)["examples"]:
+            x = np.array([float(ex["value"])], dtype=np.float32)
+            assert int(F.to_f16_bits(x)[0]) == int(ex["bits"], 16), ex["why"]
+
+
+def pin_tree_as_cache_chain(S, CM):
+    """A fully accepted chain with the tree rows attended as cached sees, at
+    node i, plain attention over the committed cache rows [0, C + i]."""
+    rng = np.random.default_rng(11)
+    hkv, hq, D, C, n = 1, 2, 64, 50, 6
+    kf = rng.standard_normal((hkv, C, D)).astype(np.float32)
+    vf = rng.standard_normal((hkv, C, D)).astype(np.float32)
+    kc = np.zeros((hkv, C + n, D // 32, 18), np.uint8)
+    vc = np.zeros_like(kc)
+    kc[:, :C] = CM.encode_rows(kf)
+    vc[:, :C] = CM.encode_rows(vf)
+    bf = lambda a: W.bf16_bits_to_f32(W.f32_to_bf16_bits(a.astype(np.float32)))
+    q, kt, vt = (bf(rng.standard_normal(sh)) for sh in ((n, hq, D), (n, hkv, D), (n, hkv, D)))
+    tokens = np.arange(n, dtype=np.int32)
+    logits = np.zeros((n, 8), np.float32)
+    for i in range(n - 1):
+        logits[i, tokens[i + 1]] = 1.0
+    res = S.verify_step(kc, vc, C, 0, q, kt, vt, np.arange(-1, n - 1, dtype=np.int32), tokens,
+                        logits, tree_as_cache=True)
+    for i in range(n):
+        keys = CM.decode_rows(kc[0, :C + i + 1])
+        vals = CM.decode_rows(vc[0, :C + i + 1])
+        for h in range(hq):
+            sc = keys @ q[i, h].astype(np.float64) / np.sqrt(D)
+            p = np.exp(sc - sc.max())
+            assert np.allclose(res["out"][i, h], p @ vals / p.sum(), rtol=1e-12, atol=1e-12)
+
+
 # ---------------------------------------------------------------- the mistakes
 
 def _real(name):
@@ -147,6 +182,15 @@ CASES = [
      [("oracle.accept", "                nxt = c\n                break\n", "                nxt = c\n")]),
     ("commit: rows one position late", pin_commit_positions,
      [("oracle.commit", "k_cache[:, ctx_len:ctx_len + L]", "k_cache[:, ctx_len + 1:ctx_len + L + 1]")]),
+    ("f16: rounding toward zero", pin_f16_golden,
+     [("oracle.f16", "return x.astype(np.float16).view(np.uint16)",
+       "h = x.astype(np.float16)\n"
+       "    h = np.where(np.abs(h.astype(np.float32)) > np.abs(x), "
+       "np.nextafter(h, np.float16(0)), h)\n"
+       "    return h.astype(np.float16).view(np.uint16)")]),
+    ("tree as cache: flag ignored", pin_tree_as_cache_chain,
+     [("oracle.step", "    if not tree_as_cache:\n        return k_tree, v_tree",
+       "    if True:\n        return k_tree, v_tree")]),
 ]
 
 
@@ -157,7 +201,9 @@ def test_pin_catches_planted_mistake(name, pin, edits):
             "pin_attention_groups": ["oracle.attention"],
             "pin_argmax_ties": ["oracle.accept"],
             "pin_walk_lowest_child": ["oracle.accept"],
-            "pin_commit_positions": ["oracle.commit", "oracle.q4_0"]}[pin.__name__]
+            "pin_commit_positions": ["oracle.commit", "oracle.q4_0"],
+            "pin_f16_golden": ["oracle.f16"],
+            "pin_tree_as_cache_chain": ["oracle.step", "oracle.commit"]}[pin.__name__]
     pin(*[_real(m) for m in mods])                     # the real oracle passes
     planted = {m: mutant(m, old, new) for m, old, new in edits}
     assert fails(pin, *[planted.get(m, _real(m)) for m in mods]), name
