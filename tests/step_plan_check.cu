@@ -1,0 +1,113 @@
+// Host-side check of the verify step's launch plan (no GPU): includes the
+// step kernel's translation unit and checks, for many problem shapes, the
+// invariants the kernel relies on. Prints one line per shape and "FAIL ..."
+// lines for violations; exit status 1 if any.
+
+#include "step.cu"
+
+#include <cstdio>
+#include <vector>
+
+namespace dfv {
+int sm_count() { return 152; }
+}
+
+using dfv::StepPlan;
+
+static int g_fail = 0;
+#define CHECK(cond, ...)                                        \
+  do {                                                          \
+    if (!(cond)) {                                              \
+      std::printf("FAIL %s: ", #cond);                          \
+      std::printf(__VA_ARGS__);                                 \
+      std::printf("\n");                                        \
+      ++g_fail;                                                 \
+    }                                                           \
+  } while (0)
+
+template <int D>
+static void stage_sizes(int& tile, int& unit_b, int& spare_b) {
+  tile = dfv::StepSmem<D>::kTileB;
+  unit_b = dfv::StepSmem<D>::kUnitStageBytes;
+  spare_b = dfv::StepSmem<D>::kSpareStageBytes;
+}
+
+static void check(int N, int hq, int hkv, int D, int W, int cap, int V, int dt, int fmt) {
+  StepPlan pl;
+  const bool ok = dfv::step_plan(N, hq, hkv, D, W, cap, V, dt, true, fmt, &pl);
+  char tag[160];
+  std::snprintf(tag, sizeof tag, "N=%d hq=%d hkv=%d D=%d W=%d cap=%d V=%d dt=%d fmt=%d", N, hq,
+                hkv, D, W, cap, V, dt, fmt);
+  if (!ok) {
+    std::printf("%s: no plan\n", tag);
+    return;
+  }
+  int tile, unit_b, spare_b;
+  if (D == 64) stage_sizes<64>(tile, unit_b, spare_b);
+  else if (D == 128) stage_sizes<128>(tile, unit_b, spare_b);
+  else stage_sizes<256>(tile, unit_b, spare_b);
+  const int esz = dt == DFV_DTYPE_BF16 ? 2 : 4;
+  CHECK(pl.grid == 152, "%s grid %d", tag, pl.grid);
+  CHECK(pl.rows == N * (hq / hkv), "%s rows", tag);
+  CHECK(pl.n_mt == (pl.rows + 127) / 128, "%s tiles", tag);
+  CHECK(pl.splits >= 1 && pl.units == hkv * pl.n_mt * pl.splits && pl.units <= pl.grid,
+        "%s units %d splits %d", tag, pl.units, pl.splits);
+  CHECK(pl.walker == (pl.grid > pl.units ? pl.grid - 1 : 0), "%s walker %d", tag, pl.walker);
+  // the walker stages every argmax partial in its Q tile
+  CHECK(static_cast<long>(pl.lunits) * static_cast<long>(sizeof(dfv::ArgPartial)) <= tile,
+        "%s lunits %d exceed the walker's staging", tag, pl.lunits);
+  if (pl.lbulk) {
+    CHECK(pl.lunits == N * pl.lchunks, "%s lunits", tag);
+    CHECK(static_cast<long>(pl.lchunk_len) * pl.lchunks >= V, "%s slices cover the vocabulary", tag);
+    CHECK((static_cast<long>(V) * esz) % 16 == 0 && (pl.lchunk_len * esz) % 16 == 0,
+          "%s slice alignment", tag);
+    CHECK(pl.lstride >= pl.lchunk_len * esz && pl.lstride % 16 == 0, "%s stride", tag);
+    std::vector<int> seen(pl.lunits, 0);
+    for (int b = 0; b < pl.grid; ++b) {
+      const int s0 = pl.lslot[b] & 0xFFFF, sn = pl.lslot[b] >> 16;
+      if (sn == 0) continue;
+      CHECK(b != pl.walker || !pl.walker_local, "%s walker %d stages slices", tag, b);
+      CHECK(sn <= dfv::kMaxStagedSlices, "%s CTA %d stages %d slices", tag, b, sn);
+      const long room = b < pl.units ? unit_b : spare_b;
+      CHECK(static_cast<long>(sn) * pl.lstride <= room, "%s CTA %d staging %ld > %ld", tag, b,
+            static_cast<long>(sn) * pl.lstride, room);
+      for (int u = s0; u < s0 + sn; ++u) {
+        CHECK(u >= 0 && u < pl.lunits, "%s CTA %d slice %d out of range", tag, b, u);
+        if (u >= 0 && u < pl.lunits) ++seen[u];
+      }
+    }
+    for (int u = 0; u < pl.lunits; ++u) CHECK(seen[u] == 1, "%s slice %d held %d times", tag, u, seen[u]);
+  } else {
+    for (int b = 0; b < pl.grid; ++b) CHECK(pl.lslot[b] == 0, "%s CTA %d stages without bulk", tag, b);
+  }
+  // workspace regions in order, 256-byte aligned
+  CHECK(pl.ws_bar == 0 && pl.ws_arg % 256 == 0 && pl.ws_qrows % 256 == 0 && pl.ws_ml % 256 == 0 &&
+            pl.ws_o % 256 == 0 && pl.ws_total % 256 == 0,
+        "%s workspace alignment", tag);
+  CHECK(pl.ws_arg >= (4 + 2 * static_cast<size_t>(hkv) * pl.n_mt + pl.units) * 4 &&
+            pl.ws_qrows >= pl.ws_arg + static_cast<size_t>(pl.lunits) * sizeof(dfv::ArgPartial) &&
+            pl.ws_ml >= pl.ws_qrows + static_cast<size_t>(N) * hkv * 2 * D * 2 &&
+            pl.ws_o >= pl.ws_ml && pl.ws_total >= pl.ws_o,
+        "%s workspace order", tag);
+  if (pl.splits > 1)
+    CHECK(pl.ws_total - pl.ws_o >= static_cast<size_t>(pl.units) * 128 * D * 2 &&
+              pl.ws_o - pl.ws_ml >= static_cast<size_t>(pl.units) * 128 * 8,
+          "%s partial sizes", tag);
+  std::printf("%s: grid %d units %d splits %d tiles %d lunits %d lbulk %d walker_local %d\n", tag,
+              pl.grid, pl.units, pl.splits, pl.n_mt, pl.lunits, pl.lbulk, pl.walker_local);
+}
+
+int main() {
+  const int heads[][2] = {{4, 1}, {8, 2}, {24, 4}, {32, 4}, {6, 6}};
+  for (int D : {64, 128, 256})
+    for (const auto& h : heads)
+      for (int N : {1, 9, 23, 49, 65})
+        for (int W : {0, 2048})
+          for (int C : {0, 4096, 61440, 131072})
+            for (int V : {1, 7, 1024, 32000, 151936, 262143, 262144})
+              for (int dt : {DFV_DTYPE_BF16, DFV_DTYPE_F32})
+                for (int fmt : {DFV_KV_Q4_0, DFV_KV_F16})
+                  check(N, h[0], h[1], D, W, C + 64 * N, V, dt, fmt);
+  std::printf("%s (%d failures)\n", g_fail ? "FAILED" : "ok", g_fail);
+  return g_fail ? 1 : 0;
+}

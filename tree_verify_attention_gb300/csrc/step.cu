@@ -1322,6 +1322,8 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
   pl->splits = static_cast<int>(s);
   pl->units = hkv * pl->n_mt * pl->splits;
   const int tile_b = kRowsPerTile * head_dim * 2;        // logits staging bytes
+  // the walker stages every argmax partial in its Q tile
+  const int max_parts = tile_b / static_cast<int>(sizeof(ArgPartial));
   const int esz = logits_dtype == DFV_DTYPE_BF16 ? 2 : 4;
   // the walker: a CTA without an attention unit when there is one
   pl->walker = with_accept ? (pl->grid > pl->units ? pl->grid - 1 : 0) : -1;
@@ -1366,7 +1368,7 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
     int best_lc = -1, best_t = 4, best_len = 0;
     long best_load = 0;
     if (static_cast<long>(vocab) * esz % 16 == 0) {
-      const int max_lc = cap_c < 4096 / n_nodes ? cap_c : 4096 / n_nodes;   // partials staged in sQ
+      const int max_lc = cap_c < max_parts / n_nodes ? cap_c : max_parts / n_nodes;
       // the lowest tier that can hold every slice (for some slice count),
       // then the slice count that puts the least work (bytes, plus a fixed
       // cost per slice) on each CTA of that tier (fewer slices on a tie)
@@ -1438,6 +1440,7 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
       int lc = pl->grid / n_nodes;
       if (lc < need_l) lc = need_l;
       if (lc > cap_c) lc = cap_c < need_l ? need_l : cap_c;
+      if (lc > max_parts / n_nodes) lc = max_parts / n_nodes;   // longer slices instead
       pl->lchunks = lc;
       pl->lunits = n_nodes * lc;
       pl->lchunk_len = (((vocab + lc - 1) / lc) + align_el - 1) / align_el * align_el;
