@@ -80,6 +80,18 @@ static void check(int N, int hq, int hkv, int D, int W, int cap, int V, int dt, 
   } else {
     for (int b = 0; b < pl.grid; ++b) CHECK(pl.lslot[b] == 0, "%s CTA %d stages without bulk", tag, b);
   }
+  // the split merge stages (max, sum) pairs and weights of its rows in the Q tile
+  if (pl.splits > 1) {
+    int worst = 0;
+    for (int mt = 0; mt < pl.n_mt; ++mt) {
+      const int rows_t = pl.rows - mt * 128 < 128 ? pl.rows - mt * 128 : 128;
+      for (int sp = 0; sp < pl.splits; ++sp) {
+        const int nr = (sp + 1) * rows_t / pl.splits - sp * rows_t / pl.splits;
+        if (nr * pl.splits > worst) worst = nr * pl.splits;
+      }
+    }
+    CHECK(worst * 12 <= tile, "%s merge staging %d bytes", tag, worst * 12);
+  }
   // workspace regions in order, 256-byte aligned
   CHECK(pl.ws_bar == 0 && pl.ws_arg % 256 == 0 && pl.ws_qrows % 256 == 0 && pl.ws_ml % 256 == 0 &&
             pl.ws_o % 256 == 0 && pl.ws_total % 256 == 0,
