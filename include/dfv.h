@@ -220,7 +220,9 @@ dfv_status dfv_greedy_accept(int n_nodes, int vocab, int logits_dtype, const voi
  *   DFV_GREEDY_ACCEPT_STATIC_SCRATCH_BYTES); nothing is launched then.
  * - The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current) and caches it; make
- *   that first call before any stream capture.
+ *   that first call before any stream capture. The cached address is tied
+ *   to the device's context: do not use the library again in a process
+ *   after cudaDeviceReset.
  * - Each call clears the part of the array that must start at zero, in
  *   stream order, before its kernel. All calls on a device share the array:
  *   calls whose work overlaps on the GPU (different streams, no ordering)

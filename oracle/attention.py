@@ -95,3 +95,61 @@ def attention_one(q_ih, k_ctx_kv, v_ctx_kv, k_tree_kv, v_tree_kv, parent,
     p = np.exp(s - mx)
     den = p.sum()
     return (p @ vals) / den, mx + np.log(den)
+
+
+def tree_verify_attention_by_head(q, k_ctx, v_ctx, k_tree, v_tree, parent, ctx_len,
+                                  window, scale=None):
+    """The same ``(out, lse)`` as ``tree_verify_attention``, computed one KV
+    head at a time with whole-matrix products instead of a loop over (node,
+    query head) pairs, so that it finishes in seconds at a context of
+    131072. The definition is unchanged: every row of a KV head's group
+    scores the committed keys of the union of the visible ranges and the
+    tree keys, the keys a row may not see get -inf (window per node depth,
+    ancestors-or-self for tree keys), then a max-subtracted softmax in
+    float64. ``k_ctx`` / ``v_ctx`` may be callables ``f(kv, lo, hi)``
+    returning the KV head's rows [lo, hi) (so that a caller can dequantise
+    one head at a time)."""
+    q = np.asarray(q, dtype=np.float64)
+    k_tree = np.asarray(k_tree, dtype=np.float64)
+    v_tree = np.asarray(v_tree, dtype=np.float64)
+    n, hq, d = q.shape
+    hkv = k_tree.shape[1]
+    if hq % hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    group = hq // hkv
+    if scale is None:
+        scale = 1.0 / np.sqrt(float(d))
+    depth = _tree.depths(parent)
+    anc = _tree.ancestors_or_self(parent)
+    ranges = [visible_committed(ctx_len, window, int(depth[i])) for i in range(n)]
+    lo_all = min(lo for lo, _ in ranges) if n else 0
+    # visibility of each row (node i, query head h within the group), row
+    # index i * group + h: committed keys [lo_all, C) then tree keys 0..N-1
+    vis_c = np.zeros((n, ctx_len - lo_all), dtype=bool)
+    for i, (lo, hi) in enumerate(ranges):
+        vis_c[i, lo - lo_all:hi - lo_all] = True
+    vis_t = np.zeros((n, n), dtype=bool)
+    for i in range(n):
+        vis_t[i, anc[i]] = True
+    vis = np.repeat(np.concatenate([vis_c, vis_t], axis=1), group, axis=0)
+
+    def rows(src, kv):
+        if callable(src):
+            return np.asarray(src(kv, lo_all, ctx_len), dtype=np.float64)
+        return np.asarray(src[kv, lo_all:ctx_len], dtype=np.float64)
+
+    out = np.zeros((n, hq, d), dtype=np.float64)
+    lse = np.zeros((n, hq), dtype=np.float64)
+    for kv in range(hkv):
+        qg = q[:, kv * group:(kv + 1) * group].reshape(n * group, d)
+        keys = np.concatenate([rows(k_ctx, kv), k_tree[:, kv]], axis=0)
+        vals = np.concatenate([rows(v_ctx, kv), v_tree[:, kv]], axis=0)
+        s = (qg @ keys.T) * scale
+        s = np.where(vis, s, -np.inf)
+        mx = s.max(axis=1, keepdims=True)
+        p = np.exp(s - mx)
+        den = p.sum(axis=1, keepdims=True)
+        o = (p @ vals) / den
+        out[:, kv * group:(kv + 1) * group] = o.reshape(n, group, d)
+        lse[:, kv * group:(kv + 1) * group] = (mx + np.log(den)).reshape(n, group)
+    return out, lse

@@ -8,8 +8,11 @@
 #include <cstdio>
 #include <vector>
 
+// The planner derives the grid, the splits, the walker and the slice
+// placement from the SM count; main() sweeps it.
+static int g_sms = 152;
 namespace dfv {
-int sm_count() { return 152; }
+int sm_count() { return g_sms; }
 }
 
 using dfv::StepPlan;
@@ -26,37 +29,58 @@ static int g_fail = 0;
   } while (0)
 
 template <int D>
-static void stage_sizes(int& tile, int& unit_b, int& spare_b) {
+static void stage_sizes(int& tile, int& spare_b, int& kbytes, int& unit_b) {
   tile = dfv::StepSmem<D>::kTileB;
-  unit_b = dfv::StepSmem<D>::kUnitStageBytes;
   spare_b = dfv::StepSmem<D>::kSpareStageBytes;
+  kbytes = dfv::StepSmem<D>::kKBytes;
+  unit_b = dfv::StepSmem<D>::kUnitStageBytes;
 }
 
 static void check(int N, int hq, int hkv, int D, int W, int cap, int V, int dt, int fmt) {
   StepPlan pl;
   const bool ok = dfv::step_plan(N, hq, hkv, D, W, cap, V, dt, true, fmt, &pl);
   char tag[160];
-  std::snprintf(tag, sizeof tag, "N=%d hq=%d hkv=%d D=%d W=%d cap=%d V=%d dt=%d fmt=%d", N, hq,
-                hkv, D, W, cap, V, dt, fmt);
+  std::snprintf(tag, sizeof tag, "sms=%d N=%d hq=%d hkv=%d D=%d W=%d cap=%d V=%d dt=%d fmt=%d",
+                g_sms, N, hq, hkv, D, W, cap, V, dt, fmt);
   if (!ok) {
     std::printf("%s: no plan\n", tag);
     return;
   }
-  int tile, unit_b, spare_b;
-  if (D == 64) stage_sizes<64>(tile, unit_b, spare_b);
-  else if (D == 128) stage_sizes<128>(tile, unit_b, spare_b);
-  else stage_sizes<256>(tile, unit_b, spare_b);
+  int tile, spare_b, kbytes, unit_b;
+  if (D == 64) stage_sizes<64>(tile, spare_b, kbytes, unit_b);
+  else if (D == 128) stage_sizes<128>(tile, spare_b, kbytes, unit_b);
+  else stage_sizes<256>(tile, spare_b, kbytes, unit_b);
   const int esz = dt == DFV_DTYPE_BF16 ? 2 : 4;
-  CHECK(pl.grid == 152, "%s grid %d", tag, pl.grid);
+  CHECK(pl.grid == (g_sms < dfv::kMaxStepGrid ? g_sms : dfv::kMaxStepGrid), "%s grid %d", tag,
+        pl.grid);
   CHECK(pl.rows == N * (hq / hkv), "%s rows", tag);
-  CHECK(pl.n_mt == (pl.rows + 127) / 128, "%s tiles", tag);
-  CHECK(pl.splits >= 1 && pl.units == hkv * pl.n_mt * pl.splits && pl.units <= pl.grid,
+  // tile groups: 128-row tiles; remainder rows <= 32 folded into the last
+  // group only with a full tile before them and head dim >= 128
+  const int full = pl.rows / 128, rem = pl.rows % 128;
+  if (pl.has_b) {
+    CHECK(D >= 128 && full >= 1 && rem > 0 && rem <= dfv::kMaxBRows, "%s remainder rows", tag);
+    CHECK(pl.n_grp == full && pl.b_rows == rem, "%s groups with remainder", tag);
+    CHECK((pl.nb == 16 || pl.nb == 32) && pl.nb >= pl.b_rows, "%s remainder N %d", tag, pl.nb);
+    CHECK(128 + D + pl.nb + (D / 128) * pl.nb <= 512, "%s TMEM columns", tag);
+  } else {
+    CHECK(pl.b_rows == 0 && pl.n_grp == full + (rem > 0 ? 1 : 0), "%s groups", tag);
+  }
+  CHECK(128 * pl.n_grp + pl.b_rows >= pl.rows && 128 * (pl.n_grp - 1) < pl.rows, "%s rows covered",
+        tag);
+  CHECK(pl.splits >= 1 && pl.units == hkv * pl.n_grp * pl.splits && pl.units <= pl.grid,
         "%s units %d splits %d", tag, pl.units, pl.splits);
   CHECK(pl.walker == (pl.grid > pl.units ? pl.grid - 1 : 0), "%s walker %d", tag, pl.walker);
   // the walker stages every argmax partial in its Q tile
   CHECK(static_cast<long>(pl.lunits) * static_cast<long>(sizeof(dfv::ArgPartial)) <= tile,
         "%s lunits %d exceed the walker's staging", tag, pl.lunits);
+  if (pl.walker_local)
+    CHECK(static_cast<long>(N) * hkv * 2 * dfv::kv_row_bytes(fmt, D) <= kbytes,
+          "%s walker's tree rows", tag);
   if (pl.lbulk) {
+    // slices are staged in rounds through the two halves of the staging area
+    CHECK(pl.lper >= 1 && pl.lper <= dfv::kMaxStagedSlices / 2 &&
+              2L * pl.lper * pl.lstride <= spare_b,
+          "%s round of %d slices of %d bytes in halves of %d", tag, pl.lper, pl.lstride, spare_b / 2);
     CHECK(pl.lunits == N * pl.lchunks, "%s lunits", tag);
     CHECK(static_cast<long>(pl.lchunk_len) * pl.lchunks >= V, "%s slices cover the vocabulary", tag);
     CHECK((static_cast<long>(V) * esz) % 16 == 0 && (pl.lchunk_len * esz) % 16 == 0,
@@ -66,11 +90,17 @@ static void check(int N, int hq, int hkv, int D, int W, int cap, int V, int dt, 
     for (int b = 0; b < pl.grid; ++b) {
       const int s0 = pl.lslot[b] & 0xFFFF, sn = pl.lslot[b] >> 16;
       if (sn == 0) continue;
-      CHECK(b != pl.walker || !pl.walker_local, "%s walker %d stages slices", tag, b);
-      CHECK(sn <= dfv::kMaxStagedSlices, "%s CTA %d stages %d slices", tag, b, sn);
-      const long room = b < pl.units ? unit_b : spare_b;
-      CHECK(static_cast<long>(sn) * pl.lstride <= room, "%s CTA %d staging %ld > %ld", tag, b,
-            static_cast<long>(sn) * pl.lstride, room);
+      CHECK(b != pl.walker, "%s the walker stages slices", tag);
+      if (b < pl.units) {
+        // a unit stages one round at entry, in the smem its tile of at most
+        // 32 real rows leaves free until its dequant
+        const int g = (b / pl.splits) % pl.n_grp;
+        const int rows_g = pl.rows - g * 128 < 128 ? pl.rows - g * 128 : 128;
+        CHECK(!pl.has_b && g == pl.n_grp - 1 && rows_g <= 32, "%s unit %d (group %d, %d rows) stages slices",
+              tag, b, g, rows_g);
+        CHECK(sn <= pl.lper && static_cast<long>(sn) * pl.lstride <= unit_b,
+              "%s unit %d stages %d slices of %d bytes in %d", tag, b, sn, pl.lstride, unit_b);
+      }
       for (int u = s0; u < s0 + sn; ++u) {
         CHECK(u >= 0 && u < pl.lunits, "%s CTA %d slice %d out of range", tag, b, u);
         if (u >= 0 && u < pl.lunits) ++seen[u];
@@ -83,8 +113,10 @@ static void check(int N, int hq, int hkv, int D, int W, int cap, int V, int dt, 
   // the split merge stages (max, sum) pairs and weights of its rows in the Q tile
   if (pl.splits > 1) {
     int worst = 0;
-    for (int mt = 0; mt < pl.n_mt; ++mt) {
-      const int rows_t = pl.rows - mt * 128 < 128 ? pl.rows - mt * 128 : 128;
+    for (int g = 0; g < pl.n_grp; ++g) {
+      const int a_rows = pl.rows - g * 128 < 128 ? pl.rows - g * 128 : 128;
+      const int rows_t = a_rows + (pl.has_b && g == pl.n_grp - 1 ? pl.b_rows : 0);
+      CHECK(rows_t <= dfv::kMaxGroupRows, "%s group rows %d", tag, rows_t);
       for (int sp = 0; sp < pl.splits; ++sp) {
         const int nr = (sp + 1) * rows_t / pl.splits - sp * rows_t / pl.splits;
         if (nr * pl.splits > worst) worst = nr * pl.splits;
@@ -93,24 +125,33 @@ static void check(int N, int hq, int hkv, int D, int W, int cap, int V, int dt, 
     CHECK(worst * 12 <= tile, "%s merge staging %d bytes", tag, worst * 12);
   }
   // workspace regions in order, 256-byte aligned
+  const size_t groups = static_cast<size_t>(hkv) * pl.n_grp;
   CHECK(pl.ws_bar == 0 && pl.ws_arg % 256 == 0 && pl.ws_qrows % 256 == 0 && pl.ws_ml % 256 == 0 &&
             pl.ws_o % 256 == 0 && pl.ws_total % 256 == 0,
         "%s workspace alignment", tag);
-  CHECK(pl.ws_arg >= (4 + 2 * static_cast<size_t>(hkv) * pl.n_mt + pl.units) * 4 &&
+  CHECK(pl.ws_arg >= (4 + 2 * groups + pl.units) * 4 &&
             pl.ws_qrows >= pl.ws_arg + static_cast<size_t>(pl.lunits) * sizeof(dfv::ArgPartial) &&
             pl.ws_ml >= pl.ws_qrows + static_cast<size_t>(N) * hkv * 2 * D * 2 &&
             pl.ws_o >= pl.ws_ml && pl.ws_total >= pl.ws_o,
         "%s workspace order", tag);
-  if (pl.splits > 1)
-    CHECK(pl.ws_total - pl.ws_o >= static_cast<size_t>(pl.units) * 128 * D * 2 &&
-              pl.ws_o - pl.ws_ml >= static_cast<size_t>(pl.units) * 128 * 8,
+  if (pl.splits > 1) {
+    // partial rows: D fp16 values + (max, sum) + padding each
+    CHECK(pl.ws_total - pl.ws_o >= static_cast<size_t>(pl.units) * dfv::kMaxGroupRows * (D * 2 + 16),
           "%s partial sizes", tag);
-  std::printf("%s: grid %d units %d splits %d tiles %d lunits %d lbulk %d walker_local %d\n", tag,
-              pl.grid, pl.units, pl.splits, pl.n_mt, pl.lunits, pl.lbulk, pl.walker_local);
+    // the merge stages (rows + splits) partial rows at most in sK + sV
+    const long merge_b = kbytes + 128L * D * 2;
+    CHECK((dfv::kMaxGroupRows + pl.splits) * static_cast<long>(D * 2 + 16) <= merge_b,
+          "%s merge staging", tag);
+  }
+  std::printf("%s: grid %d units %d splits %d groups %d rem %d lunits %d lbulk %d walker_local %d\n",
+              tag, pl.grid, pl.units, pl.splits, pl.n_grp, pl.b_rows, pl.lunits, pl.lbulk,
+              pl.walker_local);
 }
 
 int main() {
   const int heads[][2] = {{4, 1}, {8, 2}, {24, 4}, {32, 4}, {6, 6}};
+  for (int sms : {100, 132, 148, 152, 160, 256, 300}) {
+  g_sms = sms;
   for (int D : {64, 128, 256})
     for (const auto& h : heads)
       for (int N : {1, 9, 23, 49, 65})
@@ -120,6 +161,7 @@ int main() {
               for (int dt : {DFV_DTYPE_BF16, DFV_DTYPE_F32})
                 for (int fmt : {DFV_KV_Q4_0, DFV_KV_F16})
                   check(N, h[0], h[1], D, W, C + 64 * N, V, dt, fmt);
+  }
   std::printf("%s (%d failures)\n", g_fail ? "FAILED" : "ok", g_fail);
   return g_fail ? 1 : 0;
 }

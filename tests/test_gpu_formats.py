@@ -215,9 +215,10 @@ class Run:
         assert np.array_equal(k[:, sl], self.kc[:, sl])
         assert np.array_equal(v[:, sl], self.vc[:, sl])
 
-    def run(self, s, sample=None):
-        """One step on both sides; attention compared in full, or on the
-        sampled (node, query head) pairs only."""
+    def run(self, s, sample=None, by_head=False):
+        """One step on both sides; attention compared in full (with
+        ``by_head``: through the oracle's per-KV-head form, for long
+        contexts), or on the sampled (node, query head) pairs only."""
         cfg = self.cfg
         self.step.status.zero_()
         self.step.run(self.cache, bf16_dev(s.q), bf16_dev(s.k_tree), bf16_dev(s.v_tree),
@@ -228,10 +229,20 @@ class Run:
         lg = W.bf16_bits_to_f32(s.logits) if s.logits.dtype == np.uint16 else s.logits
         if sample is not None:
             self.check_sampled(s, C0, sample)
+        if by_head:
+            ka, va = oracle.step.tree_rows_attended(tree_f32(s.k_tree), tree_f32(s.v_tree),
+                                                    self.fmt, self.tq)
+            kc, vc, fmt = self.kc, self.vc, self.fmt
+            ref_out, ref_lse = oracle.attention.tree_verify_attention_by_head(
+                tree_f32(s.q), lambda kv, lo, hi: oracle.commit.decode_rows(kc[kv, lo:hi], fmt),
+                lambda kv, lo, hi: oracle.commit.decode_rows(vc[kv, lo:hi], fmt), ka, va,
+                s.parent, C0, cfg.window)
         ref = oracle.step.verify_step(self.kc, self.vc, C0, cfg.window, tree_f32(s.q),
                                       tree_f32(s.k_tree), tree_f32(s.v_tree), s.parent,
                                       s.tokens, lg, fmt=self.fmt, tree_as_cache=self.tq,
-                                      with_attention=sample is None)
+                                      with_attention=sample is None and not by_head)
+        if by_head:
+            ref["out"], ref["lse"] = ref_out, ref_lse
         self.C = ref["ctx_len"]
         st = self.step
         L = ref["accept_len"]
@@ -296,16 +307,12 @@ def test_step_f16_chained_long_context():
 
 
 @pytest.mark.parametrize("fmt,tq", [("f16", False), ("q4_0", True)])
-def test_step_ctx131072_sampled_formats(fmt, tq):
+def test_step_ctx131072_formats(fmt, tq):
     """Full 131072-token context, no window (each attention unit runs many
-    key chunks): attention checked on sampled (node, head) rows, the rest
-    bit-exactly."""
+    key chunks): every (node, query head) attention row against the oracle,
+    the rest bit-exactly."""
     cfg = W.FULL_LONG
     r = Run(cfg, cfg.ctx_len + 64, fmt, tq, check_fill=False)
     r.check_cache(slice(0, 2048))
     r.check_cache(slice(cfg.ctx_len - 2048, cfg.ctx_len))
-    s = W.make_step(cfg, 0)
-    rng = np.random.default_rng(1)
-    pairs = [(0, 0), (cfg.n_nodes - 1, cfg.n_q_heads - 1)]
-    pairs += [(int(rng.integers(cfg.n_nodes)), int(rng.integers(cfg.n_q_heads))) for _ in range(6)]
-    r.run(s, sample=pairs)
+    r.run(W.make_step(cfg, 0), by_head=True)

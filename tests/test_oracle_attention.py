@@ -101,6 +101,31 @@ def test_matches_sdpa_with_brute_force_mask(seed, window):
     ref, ref_lse = _sdpa(q, kc, vc, kt, vt, mask, C)
     np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(lse, ref_lse, rtol=1e-12, atol=1e-12)
+    # the per-KV-head matrix form, against the same brute-force reference
+    out_h, lse_h = A.tree_verify_attention_by_head(q, kc, vc, kt, vt, parent, C, window)
+    np.testing.assert_allclose(out_h, ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse_h, ref_lse, rtol=1e-12, atol=1e-12)
+
+
+def test_by_head_takes_row_callables():
+    """The per-head form reads committed rows through a callable exactly as
+    from arrays (the GPU tests pass one that dequantises a head at a time)."""
+    rng = np.random.default_rng(23)
+    n, C, W = 9, 40, 17
+    parent = _rand_tree(rng, n, 4)
+    q, kc, vc, kt, vt = _inputs(rng, n, 6, 2, 16, C)
+    calls = []
+
+    def fk(kv, lo, hi):
+        calls.append((kv, lo, hi))
+        return kc[kv, lo:hi]
+
+    out, lse = A.tree_verify_attention_by_head(q, fk, lambda kv, lo, hi: vc[kv, lo:hi], kt, vt,
+                                               parent, C, W)
+    ref, ref_lse = A.tree_verify_attention(q, kc, vc, kt, vt, parent, C, W)
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, rtol=1e-12, atol=1e-12)
+    assert calls == [(0, C - W + 1, C), (1, C - W + 1, C)]
 
 
 def test_chain_is_causal_sliding_window_decode():

@@ -66,6 +66,20 @@ def pin_attention_sdpa(A):
             assert np.allclose(lse, ref_lse, rtol=1e-10, atol=1e-12)
 
 
+def pin_attention_by_head_sdpa(A):
+    for seed in range(4):
+        for window in (0, 1, 3, 17):
+            rng = np.random.default_rng(seed)
+            n = int(rng.integers(2, 10))
+            C = int(rng.integers(4, 48))
+            parent = TA._rand_tree(rng, n, 4)
+            q, kc, vc, kt, vt = TA._inputs(rng, n, 4, 2, 16, C)
+            out, lse = A.tree_verify_attention_by_head(q, kc, vc, kt, vt, parent, C, window)
+            ref, ref_lse = TA._sdpa(q, kc, vc, kt, vt, TA._brute_mask(parent, C, window), C)
+            assert np.allclose(out, ref, rtol=1e-10, atol=1e-12)
+            assert np.allclose(lse, ref_lse, rtol=1e-10, atol=1e-12)
+
+
 def pin_attention_groups(A):
     rng = np.random.default_rng(16)
     n, C = 5, 12
@@ -174,6 +188,16 @@ CASES = [
      [("oracle.attention", "anc = _tree.ancestors_or_self(parent)\n    out = np.zeros",
        "anc = [a[:-1] if len(a) > 1 else a for a in _tree.ancestors_or_self(parent)]\n"
        "    out = np.zeros")]),
+    ("attention by head: window range one key late", pin_attention_by_head_sdpa,
+     [("oracle.attention", "vis_c[i, lo - lo_all:hi - lo_all] = True",
+       "vis_c[i, lo - lo_all + 1:hi - lo_all] = True")]),
+    ("attention by head: scale 1/D", pin_attention_by_head_sdpa,
+     [("oracle.attention", "scale = 1.0 / np.sqrt(float(d))", "scale = 1.0 / float(d)")]),
+    ("attention by head: query heads strided over KV heads", pin_attention_by_head_sdpa,
+     [("oracle.attention", "qg = q[:, kv * group:(kv + 1) * group].reshape(n * group, d)",
+       "qg = q[:, kv::hkv].reshape(n * group, d)")]),
+    ("attention by head: node excluded from its own keys", pin_attention_by_head_sdpa,
+     [("oracle.attention", "vis_t[i, anc[i]] = True", "vis_t[i, anc[i][:-1]] = True")]),
     ("argmax: last index of the maximum", pin_argmax_ties,
      [("oracle.accept", "return np.argmax(np.asarray(logits, dtype=np.float64), axis=-1).astype(np.int64)",
        "x = np.asarray(logits, dtype=np.float64)\n"
@@ -198,6 +222,7 @@ CASES = [
 def test_pin_catches_planted_mistake(name, pin, edits):
     mods = {"pin_q4_golden": ["oracle.q4_0"],
             "pin_attention_sdpa": ["oracle.attention"],
+            "pin_attention_by_head_sdpa": ["oracle.attention"],
             "pin_attention_groups": ["oracle.attention"],
             "pin_argmax_ties": ["oracle.accept"],
             "pin_walk_lowest_child": ["oracle.accept"],

@@ -14,9 +14,14 @@
 // that loads the library holds it until the process exits. Host code cannot
 // use its name as a device address, so the first call on each device looks
 // its address up with cudaGetSymbolAddress (with that device current) and
-// caches it. That first call may also load the module on the device, so it
-// should happen before any stream capture. Every call on a device uses the
-// same array; calls whose kernels overlap on the GPU race on it.
+// caches it (an atomic per device, so host threads making their first
+// calls at once agree on it). That first call may also load the module on
+// the device, so it should happen before any stream capture. The cached
+// address belongs to the device's current context: after cudaDeviceReset
+// the library must not be used again in the process. Every call on a device
+// uses the same array; calls whose kernels overlap on the GPU race on it.
+
+#include <atomic>
 
 #include "common.cuh"
 #include "accept_impl.cuh"
@@ -32,18 +37,20 @@ size_t accept_workspace_bytes(int n_nodes, int vocab);
 namespace {
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices] = {};
+std::atomic<void*> g_scratch_ptr[kMaxDevices];
 
-// Address of this device's array, looked up once per device.
+// Address of this device's array, looked up once per device. Two threads
+// racing on the first lookup both get the same address from the runtime,
+// so either store is correct.
 void* scratch_for_current_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
+  void* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
     if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess) return nullptr;
-    g_scratch_ptr[dev] = p;
+    g_scratch_ptr[dev].store(p, std::memory_order_release);
   }
-  return g_scratch_ptr[dev];
+  return p;
 }
 
 }  // namespace

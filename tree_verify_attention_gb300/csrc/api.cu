@@ -1,21 +1,25 @@
 // Library-wide entry points: status strings, version, workspace clearing,
 // device queries, and the whole verify step composed from the three parts.
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace dfv {
 
+// SMs of the current device, looked up once per device (an atomic per
+// device: concurrent first lookups store the same value).
 int sm_count() {
-  static int cached[64] = {};
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (cached[dev] == 0) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
       n = 148;
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 size_t step_workspace_bytes(int n_nodes, int hq, int hkv, int head_dim, int window, int cap,

@@ -14,9 +14,32 @@ namespace dfv {
 
 constexpr int kMaxNodes = DFV_MAX_NODES;
 constexpr int kMaskWords = (kMaxNodes + 31) / 32;   // 3
-// Bound on polling iterations of any wait (each try_wait may also suspend
-// in hardware for a while); reaching it sets DFV_DEV_TIMEOUT.
-constexpr uint32_t kWaitLimit = 1u << 26;
+// Every wait in the library gives up after kWaitNs nanoseconds of the GPU's
+// global timer (far above any step's duration) and sets DFV_DEV_TIMEOUT;
+// kWaitPolls bounds the polls as well, in case the timer stood still.
+constexpr uint64_t kWaitNs = 100ull * 1000 * 1000;   // 100 ms
+constexpr uint32_t kWaitPolls = 1u << 30;
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Polls `done()` until it returns true (then true) or the time limit
+// passes (then false). The timer is read once every 64 polls.
+template <typename F>
+__device__ __forceinline__ bool wait_bounded(F done) {
+  if (done()) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 0; it < kWaitPolls; it += 64) {
+#pragma unroll 1
+    for (int k = 0; k < 64; ++k)
+      if (done()) return true;
+    if (global_ns() - t0 > kWaitNs) return false;
+  }
+  return false;
+}
 
 __device__ __forceinline__ void report(uint32_t* status, uint32_t bits) {
   if (status != nullptr) atomicOr(status, bits);
@@ -74,11 +97,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait; false if the limit was reached.
+// Bounded wait (kWaitNs); false if the limit was reached.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-  for (uint32_t it = 0; it < kWaitLimit; ++it)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
+  return wait_bounded([&]() { return mbar_try_wait(bar, parity); });
 }
 
 // 1-D bulk copy global -> shared through the TMA engine, completing
@@ -91,6 +112,25 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
           "r"(smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// 1-D bulk copy shared -> global through the TMA engine, in this thread's
+// bulk async-group; bulk_commit_wait() commits the group and waits until its
+// writes are complete. dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_wait() {
+  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Orders this thread's global accesses through the generic proxy with those
+// through the async proxy (bulk copies), both ways.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- tensor core (legacy path)

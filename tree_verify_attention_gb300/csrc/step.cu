@@ -9,28 +9,32 @@
 // greedy walk, and the commit of the accepted rows in the cache format.
 //
 // One CTA per SM, one launch per step, no grid-wide barrier. CTA roles:
-//   * attention units = (KV head h, 128-row tile of the head's (node, query
-//     head) rows, range of 128-key chunks); the tree chunk is processed
-//     first, by the last split of each (head, tile) group;
-//   * CTAs without a unit scan logits slices (the units of short row tiles
-//     take the rest); one of them is the walker.
-// At t = 0 thread 0 starts 1-D bulk copies (TMA engine) of the CTA's first
-// K / V chunk and its logits slices, and every thread loads its share of
-// the bf16 Q rows and tree rows, so that the latencies overlap. Then:
-//   * the logits slices are scanned from shared memory into (max, lowest
-//     index) partials; the tree rows are quantised into a staging area so
+//   * attention units = (KV head h, tile group of the head's (node, query
+//     head) rows, range of 128-key chunks). A tile group is a 128-row tile
+//     and, in the last group, up to 32 remainder rows (the budget-22 step
+//     has 138 rows per KV head: 128 + 10), so that every K / V chunk is
+//     loaded and decoded once for all of a head's rows. The tree chunk is
+//     processed first, by the last split of each group;
+//   * CTAs without a unit scan the logits; one of them is the walker.
+// At t = 0 thread 0 reads ctx and starts 1-D bulk copies (TMA engine) of
+// the unit's first K / V chunk (or of the CTA's logits slices), while the
+// other warps load the bf16 Q rows and the tree rows. Then:
+//   * CTAs without a unit scan their staged logits slices into (max, lowest
+//     index) partials; the walker quantises the tree rows into its smem so
 //     that the commit after the walk is a plain copy;
-//   * per chunk: Q -> fp16, K and V decoded ((q - 8) * d, one rounding; or
-//     binary16 rows copied as they are) into 128-byte-swizzled smem;
-//     S = Q K^T by tcgen05.mma into TMEM (M = 128 rows, N = 128 keys,
-//     K = D); four threads per row read S from TMEM, mask (window,
-//     ancestors), exchange the row max, exp2, write P (fp16); O += P V by
-//     tcgen05.mma (M = 128, N = D, K = 128 keys; V as an MN-major
-//     operand). The running max only moves (O rescaled in TMEM) when a
-//     chunk's max exceeds it by more than 2^8, so P <= 256 fits fp16;
-//   * each split writes its normalised O (fp16), max and sum to the
-//     workspace and marks its ready word; the splits of a group wait for
-//     one another (bounded waits) and each merges a share of the group's
+//   * per chunk: K and V decoded ((q - 8) * d, one rounding; or binary16 rows
+//     copied as they are) into 128-byte-swizzled smem; by tcgen05.mma into
+//     TMEM: S = Q K^T for the 128-row tile (M = 128 rows, N = 128 keys,
+//     K = D) and, for the remainder rows, the transposed S_B^T = K Q_B^T
+//     (M = 128 keys, N = 16 or 32 rows); the masked (window, ancestors)
+//     online softmax of both; then O += P V (M = 128, N = D, K = 128 keys; V
+//     as an MN-major operand) and O_B^T += V^T P_B^T (M = 128 head dims,
+//     N = 16 or 32 rows; V^T is the same smem tile read as an MN-major A).
+//     A running max only moves (O rescaled in TMEM) when a chunk's max
+//     exceeds it by more than 2^8, so P <= 256 fits fp16;
+//   * each split writes its normalised O rows (fp16), max and sum to the
+//     workspace and marks its ready word; the splits of a group wait for one
+//     another (time-bounded waits) and each merges a share of the group's
 //     rows by log-sum-exp;
 //   * the walker waits until every other CTA has read ctx and written its
 //     partials, merges the argmax partials, walks the tree in one warp,
@@ -49,18 +53,23 @@
 namespace dfv {
 
 constexpr int kStepThreads = 512;   // 16 warps; four per TMEM lane quadrant
-constexpr int kRowsPerTile = 128;   // UMMA M
+constexpr int kRowsPerTile = 128;   // UMMA M of a row tile
 constexpr int kChunk = 128;         // keys per chunk (UMMA N of S, K of P V)
+constexpr int kMaxBRows = 32;       // remainder rows of a tile group (UMMA N of the transposed pair)
+constexpr int kMaxGroupRows = kRowsPerTile + kMaxBRows;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxStepSplits = 256;
 constexpr int kMaxStepGrid = 256;   // CTAs of one launch at most
 constexpr int kMaxStagedSlices = 8; // logits slices one CTA stages at most
-constexpr long kSliceCostBytes = 8192;   // per-slice scan overhead, in bytes of streaming
+constexpr long kSliceCostBytes = 65536;  // per-slice scan overhead (a CTA-wide reduction), in bytes of streaming
+constexpr int kLongSpares = 8;      // CTAs left to the logits when the attention could use every SM
+constexpr bool kFoldRemainder = false;   // fold remainder rows into the last tile group
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kLogitVecs = 16;      // 16-byte logits vectors a thread keeps in flight
 
 struct StepPlan {
-  int rows, n_mt, splits, units, grid, lunits, lchunks, lchunk_len, lbulk, lstride, smem;
+  int rows, n_grp, has_b, b_rows, nb, splits, units, grid, lunits, lchunks, lchunk_len, lbulk,
+      lstride, lper, smem;
   int walker, walker_local;
   uint32_t lslot[kMaxStepGrid];   // per CTA: first logits slice | count << 16
   size_t ws_bar, ws_arg, ws_qrows, ws_ml, ws_o, ws_total;
@@ -68,8 +77,13 @@ struct StepPlan {
 
 struct StepParams {
   int n_nodes, max_depth, hq, hkv, group, window, capacity, vocab, logits_dtype;
-  int rows, n_mt, splits, units, lunits, lchunks, lchunk_len, lbulk;
+  int rows;          // N * group: (node, query head) rows of one KV head
+  int n_grp;         // tile groups per KV head
+  int has_b;         // the last group also holds remainder rows [128 * n_grp, rows)
+  int b_rows, nb;    // remainder rows, and their UMMA N (16 or 32)
+  int splits, units, lunits, lchunks, lchunk_len, lbulk;
   int lstride;       // bytes between staged slices
+  int lper;          // staged slices per half of the staging area (one round)
   uint32_t group_m;  // ceil(2^32 / group) (0 when group == 1): row -> node by multiply-high
   int do_accept;
   int tree_q;        // attend Q4_0-quantised-and-dequantised tree rows
@@ -92,36 +106,55 @@ struct StepParams {
   int32_t* accept_len;
   int32_t* path;
   int32_t* out_tokens;
-  unsigned int* bar;        // [2] CTAs done with ctx and their argmax partial
-                            // (the walker resets it); [4 + 2 g]: arrivals
-                            // (low 16 bits) and generation of split group g
+  unsigned int* bar;        // [2] CTAs done with ctx and their argmax partials
+                            // (the walker waits for exactly grid - 1 reports,
+                            // then resets it); [4 + 2 g]: arrivals (low 16
+                            // bits) and generation of split group g
   unsigned int* ready;      // [units] generation + 1 once the unit's partial is written
   ArgPartial* arg_part;     // [lunits]
   uint8_t* qrows;           // [N][Hkv][2][row bytes]
-  float2* part_ml;          // [units][128]  (running max, log2 units; sum)
-  __half* part_o;           // [units][128][D]  O / sum
+  uint8_t* part;            // [units][kMaxGroupRows] rows of kPartRowBytes: O / sum (fp16),
+                            // then (running max, log2 units; sum)
   uint32_t* status;
   uint32_t lslot[kMaxStepGrid];   // per CTA: first staged logits slice | count << 16
 };
+
+// One row of a split's partial: D fp16 values, the row's (max, sum), 8
+// bytes of padding (rows stay 16-byte aligned; consecutive rows of a staged
+// tile fall on different banks).
+template <int D>
+constexpr int kPartRowBytes = D * 2 + 16;
 
 // Dynamic shared memory map (bytes from a 1024-aligned base).
 template <int D>
 struct StepSmem {
   static constexpr int kRowB = D / 32 * 18;
   static constexpr bool kBulk = (kRowB % 16) == 0;
-  static constexpr int kTileB = kRowsPerTile * D * 2;           // one [128][D] fp16 tile
-  static constexpr int kQ = 0;          // Q fp16 (swizzled); logits slice before that
-  static constexpr int kK = kQ + kTileB;  // K^ ; raw V lands here first; P later
-  static constexpr int kKBytes = kChunk * (D > kChunk ? D : kChunk) * 2;
-  static constexpr int kV = kK + kKBytes;  // V^ ; bf16 Q rows land here first
-  static constexpr int kRawK = kV + kTileB;
-  static constexpr int kBars = kRawK + (kBulk ? kChunk * kRowB : 0);
-  // logits staging: an attention unit from past the raw V rows in sK to the
-  // end of sV, a CTA without a unit from sQ to the end of sV
-  static constexpr int kUnitStage = kK + (kBulk ? kChunk * kRowB : 0);
-  static constexpr int kUnitStageBytes = kRawK - kUnitStage;
-  static constexpr int kSpareStageBytes = kRawK;
-  static constexpr int kBytes = kBars + 64 + 1024;   // + alignment slack
+  static constexpr bool kHasB = D >= 128;   // remainder rows: O_B^T needs M = 128 head dims
+  static constexpr int kTileB = kRowsPerTile * D * 2;        // one [128][D] fp16 tile
+  static constexpr int kQ = 0;                               // Q of the 128-row tile
+  static constexpr int kK = kQ + kTileB;                     // K^, then P (and P_B past it)
+  static constexpr int kPB = kChunk * kChunk * 2;            // P_B's offset in sK
+  static constexpr int kKBytes0 = kChunk * D * 2;
+  static constexpr int kKBytes1 = kPB + (kHasB ? kMaxBRows * kChunk * 2 : 0);
+  static constexpr int kKBytes = kKBytes0 > kKBytes1 ? kKBytes0 : kKBytes1;
+  static constexpr int kV = kK + kKBytes;                    // V^; raw K, raw V land at its end first
+  static constexpr int kRawK = kChunk * D * 2 - 2 * kChunk * kRowB;   // raw K's offset in sV
+  static constexpr int kRawV = kRawK + kChunk * kRowB;                // raw V's offset in sV
+  static constexpr int kQStage = kK;                         // bf16 Q rows land here (sK, then sV)
+  static constexpr int kQB = kV + kChunk * D * 2;            // Q of the remainder rows
+  static constexpr int kQBBytes = kHasB ? kMaxBRows * D * 2 : 0;
+  static constexpr int kBars = kQB + kQBBytes;
+  static constexpr int kSpareStageBytes = kQB;               // logits staging of a CTA without a unit
+  // logits staging of a unit whose tile has at most kMaxBRows real rows:
+  // past its staged Q rows, up to the raw K / V (free until the dequant)
+  static constexpr int kUnitStage = kK + kMaxBRows * D * 2;
+  static constexpr int kUnitStageBytes = kV + kRawK - kUnitStage;
+  static constexpr int kBytes = kBars + 64 + 1024;           // + alignment slack
+  static_assert(2 * kChunk * kRowB <= kChunk * D * 2, "raw K and V fit in sV");
+  static_assert(kRawK % 16 == 0 && kRawV % 16 == 0, "bulk-copy destinations 16-byte aligned");
+  static_assert(kMaxGroupRows * D * 2 <= kKBytes + kRawK, "staged Q rows stay clear of raw K / V");
+  static_assert(kMaxGroupRows * (D * 2 + 16) <= kV, "epilogue staging fits in sQ + sK");
 };
 
 // ---------------------------------------------------------------- small helpers
@@ -182,18 +215,13 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const unsigned int* a) {
   return v;
 }
 
-// Waits (bounded) until ready[0..n) all hold `tag`; one warp polls, lane i
-// the words i, i + 32, ...; false on timeout.
+// Waits (time-bounded) until ready[0..n) all hold `tag`; one warp polls,
+// lane i the words i, i + 32, ...; false on timeout.
 __device__ __forceinline__ bool wait_ready(const unsigned int* ready, int n, uint32_t tag) {
   const int lane = threadIdx.x & 31;
   bool ok = true;
-  for (int i = lane; i < n; i += 32) {
-    uint32_t it = 0;
-    while (ld_acquire_gpu(ready + i) != tag) {
-      if (++it > (1u << 22)) { ok = false; break; }
-    }
-    if (!ok) break;
-  }
+  for (int i = lane; i < n && ok; i += 32)
+    ok = wait_bounded([&]() { return ld_acquire_gpu(ready + i) == tag; });
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -231,25 +259,58 @@ __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int* s_
 
 // ---------------------------------------------------------------- the kernel
 
-// Argmax partials of this CTA's staged logits slices [ls0, ls0 + lsn) (slice
-// k at lstage + k * lstride), once their copies have landed. One pass per
-// slice: four independent chains per thread, each keeping its running
-// maximum and the first vector that reached it; then the lowest vector
-// holding the thread's maximum is re-read for the lowest element index, and
-// the (max, lowest index) pairs merge across the CTA.
+// Thread 0: the bulk copies of round r of this CTA's staged logits slices
+// [ls0, ls0 + lsn): slices r * lper .. into half (r & 1) of the staging
+// area, completing on bars[r & 1].
 template <typename LT>
-__device__ __noinline__ void scan_slices(const StepParams& p, const uint8_t* lstage, int ls0, int lsn,
-                                         uint64_t* bar_lg, int* s_ok) {
+__device__ __forceinline__ void issue_slices(const StepParams& p, uint8_t* lstage, int ls0, int lsn, int r,
+                                             uint64_t* bars) {
+  constexpr int esz = static_cast<int>(sizeof(LT));
+  const int k0 = r * p.lper, k1 = min(lsn, k0 + p.lper);
+  uint8_t* buf = lstage + (r & 1) * p.lper * p.lstride;
+  uint32_t total = 0;
+  for (int k = k0; k < k1; ++k) {
+    const int ch = (ls0 + k) % p.lchunks;
+    const int b0 = ch * p.lchunk_len, b1 = max(b0, min(p.vocab, b0 + p.lchunk_len));
+    total += static_cast<uint32_t>((b1 - b0) * esz);
+  }
+  fence_proxy_async_smem();   // the buffer was last read through the generic proxy
+  mbar_arrive_expect_tx(bars + (r & 1), total);
+  for (int k = k0; k < k1; ++k) {
+    const int u = ls0 + k, node = u / p.lchunks, ch = u % p.lchunks;
+    const int b0 = ch * p.lchunk_len, b1 = max(b0, min(p.vocab, b0 + p.lchunk_len));
+    if (b1 > b0)
+      bulk_g2s(buf + (k - k0) * p.lstride,
+               static_cast<const uint8_t*>(p.logits) + (static_cast<size_t>(node) * p.vocab + b0) * esz,
+               static_cast<uint32_t>((b1 - b0) * esz), bars + (r & 1));
+  }
+}
+
+// Argmax partials of this CTA's staged logits slices [ls0, ls0 + lsn),
+// round by round: rounds 0 and 1 were issued at entry into the two halves
+// of the staging area, round r + 2 is issued into the half round r frees.
+// One pass per slice: four independent chains per thread, each keeping its
+// running maximum and the first vector that reached it; then the lowest
+// vector holding the thread's maximum is re-read for the lowest element
+// index, and the (max, lowest index) pairs merge across the CTA.
+template <typename LT>
+__device__ __forceinline__ void scan_slices(const StepParams& p, uint8_t* lstage, int ls0, int lsn,
+                                         uint64_t* bars, int* s_ok) {
   constexpr int esz = static_cast<int>(sizeof(LT));
   const int tid = threadIdx.x;
-  const bool ok = cta_wait(bar_lg, 0, s_ok, p.status);
+  const int rounds = (lsn + p.lper - 1) / p.lper;
 #pragma unroll 1
-  for (int k = 0; k < lsn; ++k) {
+  for (int rd = 0; rd < rounds; ++rd) {
+  const bool ok = cta_wait(bars + (rd & 1), (rd >> 1) & 1, s_ok, p.status);
+  const int k0 = rd * p.lper, k1 = min(lsn, k0 + p.lper);
+#pragma unroll 1
+  for (int k = k0; k < k1; ++k) {
     const int u = ls0 + k;
     const int lbegin = (u % p.lchunks) * p.lchunk_len;
     const int lend = max(lbegin, min(p.vocab, lbegin + p.lchunk_len));
     const int lnvec = (lend - lbegin) * esz / 16;
-    const uint4* sv = reinterpret_cast<const uint4*>(lstage + k * p.lstride);
+    const uint4* sv = reinterpret_cast<const uint4*>(lstage + (rd & 1) * p.lper * p.lstride +
+                                                     (k - k0) * p.lstride);
     float best = -INFINITY;
     int bidx = INT_MAX;
     if (ok) {
@@ -306,13 +367,15 @@ __device__ __noinline__ void scan_slices(const StepParams& p, const uint8_t* lst
       p.arg_part[u].idx = bidx;
     }
     __syncthreads();   // the staging buffer is free again
-    }
+  }
+  if (tid == 0 && rd + 2 < rounds) issue_slices<LT>(p, lstage, ls0, lsn, rd + 2, bars);
+  }
 }
 
 // Argmax partials of logits slices blk, blk + G, ... by plain loads (when the
 // slices cannot be staged in smem).
 template <typename LT>
-__device__ __noinline__ void plain_slices(const StepParams& p, int blk, int G) {
+__device__ __forceinline__ void plain_slices(const StepParams& p, int blk, int G) {
   for (int u = blk; u < p.lunits; u += G) {
     const int node = u / p.lchunks, ch = u % p.lchunks;
     const int begin = ch * p.lchunk_len;
@@ -333,7 +396,7 @@ __device__ __noinline__ void plain_slices(const StepParams& p, int blk, int G) {
 // Q4_0 blocks [b0, b1) of the tree's key / value rows, laid out
 // [node][Hkv][K, V][row bytes] at qdst.
 template <int D, int FMT>
-__device__ __noinline__ void prequant_tree(const StepParams& p, uint8_t* qdst, int b0, int b1) {
+__device__ __forceinline__ void prequant_tree(const StepParams& p, uint8_t* qdst, int b0, int b1) {
   constexpr int NB = D / 32;
   constexpr int kRowB = kv_row_bytes(FMT, D);
   if constexpr (FMT == DFV_KV_F16) {
@@ -380,26 +443,30 @@ __device__ __noinline__ void prequant_tree(const StepParams& p, uint8_t* qdst, i
 // owes (argmax partials, tree rows), merges the argmax partials per node,
 // walks the tree from the root and commits the accepted rows to the cache.
 template <int D, int FMT>
-__device__ __noinline__ void walker_tail(const StepParams& p, int G, int C, bool ctx_ok, uint8_t* sQ,
+__device__ __forceinline__ void walker_tail(const StepParams& p, int G, int C, bool ctx_ok, uint8_t* sQ,
                                          const uint8_t* sK, const int* s_wpar, const int* s_wtok) {
   using L = StepSmem<D>;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int N = p.n_nodes;
   __shared__ int s_ok;
   if (tid == 0) {
+    // exactly G - 1 reports (one per other CTA); a count that never equals
+    // it (a corrupted workspace) ends in a timeout, and nothing is committed
     volatile unsigned int* done = p.bar + 2;
-    uint32_t it = 0;
-    int ok = 1;
-    while (*done < static_cast<unsigned int>(G - 1)) {
-      if (++it > (1u << 24)) { ok = 0; break; }
+    const unsigned int want = static_cast<unsigned int>(G - 1);
+    const bool ok = wait_bounded([&]() {
+      if (*done == want) return true;
       __nanosleep(32);
-    }
+      return false;
+    });
     __threadfence();
     *done = 0u;                        // ready for the next launch
+    p.bar[3] = 0u;                     // the units' "copies issued" count too
     if (!ok) report(p.status, DFV_DEV_TIMEOUT);
-    s_ok = ok;
+    s_ok = ok ? 1 : 0;
   }
   __syncthreads();
+  if (!s_ok) return;
   __shared__ int s_am[kMaxNodes];
   __shared__ int s_path[kMaxNodes];
   __shared__ int s_L;
@@ -507,17 +574,23 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
   uint8_t* sQ = smem + L::kQ;
   uint8_t* sK = smem + L::kK;
   uint8_t* sV = smem + L::kV;
-  uint8_t* sRawK = smem + L::kRawK;
+  uint8_t* sQB = smem + L::kQB;
   uint64_t* bar_kv = reinterpret_cast<uint64_t*>(smem + L::kBars);
   uint64_t* bar_mma = bar_kv + 1;
-  uint64_t* bar_lg = bar_kv + 2;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_kv + 3);
+  uint64_t* bar_lg = bar_kv + 2;     // bar_lg[0..1]: the two halves of the logits staging
+  uint64_t* bar_lg2 = bar_kv + 3;
+  uint64_t* bar_q = bar_kv + 4;
+  uint64_t* bar_mmab = bar_kv + 5;   // the remainder rows' MMAs
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_kv + 6);
 
   __shared__ int s_J[kMaxNodes], s_dep[kMaxNodes];
   __shared__ uint32_t s_anc[kMaxNodes][kMaskWords];
   __shared__ int s_row_node[kRowsPerTile], s_row_lo[kRowsPerTile];
+  __shared__ int s_brow_node[kMaxBRows], s_brow_lo[kMaxBRows];
   __shared__ float s_pmax[4][kRowsPerTile];
-  __shared__ float s_m[kRowsPerTile], s_l[4][kRowsPerTile];
+  __shared__ float s_bmax[4][kMaxBRows];
+  __shared__ float s_l[4][kRowsPerTile];
+  __shared__ float s_bm[kMaxBRows], s_bl[4][kMaxBRows];
   __shared__ int s_ok;
   __shared__ int s_wpar[kMaxNodes], s_wtok[kMaxNodes];
 
@@ -532,13 +605,14 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
 
   // ---- this CTA's attention unit
   const int unit = blk < p.units ? blk : -1;
-  int h = 0, mt = 0, split = 0;
+  int h = 0, grp = 0, split = 0;
   if (unit >= 0) {
     split = unit % p.splits;
-    mt = (unit / p.splits) % p.n_mt;
-    h = unit / (p.splits * p.n_mt);
+    grp = (unit / p.splits) % p.n_grp;
+    h = unit / (p.splits * p.n_grp);
   }
-  constexpr int esz = static_cast<int>(sizeof(LT));   // logits element bytes
+  // the last tile group also holds the remainder rows, by transposed MMAs
+  const bool ub = L::kHasB && unit >= 0 && p.has_b && grp == p.n_grp - 1;
   // the context length, read once by thread 0 (with acquire semantics, so
   // that its report to the walker below cannot overtake it) and shared
   // through smem after the first barrier
@@ -565,23 +639,36 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
   };
 
   auto issue_kv = [&](int cc) {
-    // raw K -> sRawK, raw V -> sK (consumed before K is dequantised)
+    // raw K -> sV, raw V -> sV + kRawV (both read into registers before V^
+    // is written over them)
     const int j0 = lo_min + cc * kChunk;
     const int nk = min(kChunk, C - j0);
     const uint32_t bytes = static_cast<uint32_t>(nk * L::kRowB);
     const size_t off = (static_cast<size_t>(h) * p.capacity + j0) * L::kRowB;
     fence_proxy_async_smem();
     mbar_arrive_expect_tx(bar_kv, 2 * bytes);
-    bulk_g2s(sRawK, p.k_cache + off, bytes, bar_kv);
-    bulk_g2s(sK, p.v_cache + off, bytes, bar_kv);
+    bulk_g2s(sV + L::kRawK, p.k_cache + off, bytes, bar_kv);
+    bulk_g2s(sV + L::kRawV, p.v_cache + off, bytes, bar_kv);
+  };
+  // the tile group's rows [128 grp, 128 grp + rows_g): node n's query heads
+  // of KV head h are contiguous, so one bulk copy per node lands the bf16
+  // rows in order at sK (then on into sV, clear of the raw K / V)
+  const int a_rows_g = unit >= 0 ? min(kRowsPerTile, p.rows - grp * kRowsPerTile) : 0;
+  const int rows_g = a_rows_g + (ub ? p.b_rows : 0);
+  auto issue_q = [&]() {   // by the 32 lanes of warp 0, node n0 + lane + 32 k each
+    const int start = grp * kRowsPerTile, end = start + rows_g;
+    for (int n = div_small(start, p.group_m) + lane; n * p.group < end; n += 32) {
+      const int j0 = max(start, n * p.group) - n * p.group, j1 = min(end, (n + 1) * p.group) - n * p.group;
+      bulk_g2s(smem + L::kQStage + static_cast<size_t>(n * p.group + j0 - start) * D * 2,
+               p.q + (static_cast<size_t>(n) * p.hq + h * p.group + j0) * D,
+               static_cast<uint32_t>((j1 - j0) * D * 2), bar_q);
+    }
   };
 
-  // The logits slices [ls0, ls0 + lsn) of this CTA land in smem by TMA at
-  // t = 0 (slice k at lstage + k * lstride) and are scanned as soon as they
-  // have landed: an attention unit stages them past its raw V rows in sK and
-  // on into sV (Q goes straight to sQ; K^ and V^ wait for the scan), a CTA
-  // without a unit from sQ on. When the slices cannot be staged, every CTA
-  // takes slices blk, blk + G, ... with plain loads instead.
+  // The logits slices [ls0, ls0 + lsn) of a CTA without a unit land in smem
+  // by TMA at t = 0 (slice k at sQ + k * lstride) and are scanned as soon as
+  // they have landed. When the slices cannot be staged, every CTA takes
+  // slices blk, blk + G, ... with plain loads instead.
   const uint32_t le = p.do_accept && p.lbulk ? p.lslot[blk] : 0u;
   const int ls0 = static_cast<int>(le & 0xFFFFu), lsn = static_cast<int>(le >> 16);
   const bool lreg = lsn > 0;
@@ -593,12 +680,6 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
   const bool qshare = p.do_accept && !p.walker_local;
   const bool has_slices = lreg || (p.do_accept && !p.lbulk && blk < p.lunits);
   const bool late_signal = has_slices || qshare;
-  auto slice_range = [&](int u, int& begin, int& end) {
-    const int ch = u % p.lchunks;
-    begin = ch * p.lchunk_len;
-    end = min(p.vocab, begin + p.lchunk_len);
-    if (end < begin) end = begin;
-  };
   // the late report: after a barrier that follows every write of the CTA
   auto signal_done = [&]() {
     if (p.do_accept && blk != p.walker && tid == 0) {
@@ -609,44 +690,6 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
 
   // ================================================================ phase A
   unsigned int arrive_old = 0;   // thread 0: its add to the split group's word
-  // the last split's tree rows (its first chunk): this thread's first TP
-  // 16-byte pieces, loaded now and converted when the chunk is built
-  constexpr int TP = 4;
-  const bool tree_split = unit >= 0 && split == p.splits - 1;
-  const int nt_all = min(kChunk, N);
-  const int tree_real = 2 * nt_all * (D / 8);     // 16-byte pieces with data
-  uint4 tv[TP];
-#pragma unroll
-  for (int u = 0; u < TP; ++u) {
-    const int it = tid + u * kStepThreads;
-    tv[u] = make_uint4(0u, 0u, 0u, 0u);
-    if (tree_split && it < tree_real) {
-      const int ka = it / (D / 8), c = it % (D / 8);
-      const int kvi = ka >= nt_all ? 1 : 0, key = ka - kvi * nt_all;
-      tv[u] = __ldg(reinterpret_cast<const uint4*>(
-          (kvi ? p.tree_v : p.tree_k) + (static_cast<size_t>(key) * p.hkv + h) * D + c * 8));
-    }
-  }
-  // Q: this thread's 16-byte pieces of the tile's bf16 rows, converted into
-  // the fp16 swizzled tile (sQ) before the first barrier; rows past the
-  // last are zero
-  constexpr int QU = kRowsPerTile * (D / 8) / kStepThreads;
-  static_assert(QU >= 1, "Q pieces per thread");
-  uint4 qv[QU];
-  if (unit >= 0) {
-#pragma unroll
-    for (int u = 0; u < QU; ++u) {
-      const int it = tid + u * kStepThreads;
-      const int lr = it / (D / 8), c = it % (D / 8);
-      const int rg = mt * kRowsPerTile + lr;
-      qv[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (rg < p.rows) {
-        const int node = div_small(rg, p.group_m), j = rg - node * p.group;
-        qv[u] = __ldg(reinterpret_cast<const uint4*>(
-            p.q + (static_cast<size_t>(node) * p.hq + h * p.group + j) * D + c * 8));
-      }
-    }
-  }
   // Thread 0: the read of ctx, the split group's arrival and the first K / V
   // copy. Everything a step reads or writes that the previous step may
   // write (ctx, the cache, the outputs) comes after this.
@@ -666,39 +709,68 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       if (first_kv) issue_kv(c0);
     }
   };
-  // Thread 0, once every thread's Q and tree loads are in flight: barriers,
-  // the read of ctx and the first K / V copy (not yet when pipelined), the
-  // logits copies. (Its barrier-init fence waits for its own loads above;
-  // issuing the copies before any load was measured slower, since the
-  // first barrier then waits longer for warp 0's Q pieces.)
-  if (tid == 0) {
-    mbar_init(bar_kv, 1);
-    mbar_init(bar_mma, 1);
-    mbar_init(bar_lg, 1);
-    fence_mbar_init();
-    if (!p.pipelined) ctx_and_first_kv();
-    // the logits copies go after the K/V copy, which is on the critical path
-    if (lreg) {
-      uint32_t total = 0;
-      for (int k = 0; k < lsn; ++k) {
-        int b0, b1;
-        slice_range(ls0 + k, b0, b1);
-        total += static_cast<uint32_t>((b1 - b0) * esz);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(bar_lg, total);
-      for (int k = 0; k < lsn; ++k) {
-        const int u = ls0 + k, node = u / p.lchunks;
-        int b0, b1;
-        slice_range(u, b0, b1);
-        if (b1 > b0)
-          bulk_g2s(lstage + k * p.lstride,
-                   static_cast<const uint8_t*>(p.logits) + (static_cast<size_t>(node) * p.vocab + b0) * esz,
-                   static_cast<uint32_t>((b1 - b0) * esz), bar_lg);
-      }
+  // Warp 0 first, before any load of its own (the barrier-init fence would
+  // wait for them). Thread 0: the barriers; the read of ctx and the first K /
+  // V copy (not yet when pipelined); then warp 0's lanes issue the Q rows'
+  // copies, and, on a CTA without a unit, thread 0 the logits copies. Those
+  // wait (non-pipelined) until every unit has issued its K / V and Q copies,
+  // so that the attention's bytes are ahead of the logits in the memory
+  // system; the walker resets the count. Meanwhile warps 1..15 load the tree
+  // rows, allocate TMEM and build the tree masks; a CTA-wide barrier then
+  // makes the barriers and ctx visible to all.
+  if (warp == 0) {
+    if (tid == 0) {
+      mbar_init(bar_kv, 1);
+      mbar_init(bar_mma, 1);
+      mbar_init(bar_lg, 1);
+      mbar_init(bar_q, 1);
+      mbar_init(bar_mmab, 1);
+      mbar_init(bar_lg2, 1);
+      fence_mbar_init();
+      if (!p.pipelined) ctx_and_first_kv();
+      if (unit >= 0) mbar_arrive_expect_tx(bar_q, static_cast<uint32_t>(rows_g * D * 2));
     }
-    // nothing for the walker to wait for but the read of ctx above
-    if (!p.pipelined && p.do_accept && blk != p.walker && !late_signal) atomicAdd(p.bar + 2, 1u);
+    __syncwarp();
+    if (unit >= 0) issue_q();
+    __syncwarp();
+    if (tid == 0) {
+      if (unit >= 0 && !p.pipelined && p.do_accept) atomicAdd(p.bar + 3, 1u);
+      if (lreg) {
+        if (!p.pipelined && unit < 0) {
+          volatile unsigned int* issued = p.bar + 3;
+          const unsigned int want = static_cast<unsigned int>(p.units);
+          wait_bounded([&]() {
+            if (*issued >= want) return true;
+            __nanosleep(64);
+            return false;
+          });   // ordering only: the copies below go ahead either way
+        }
+        issue_slices<LT>(p, lstage, ls0, lsn, 0, bar_lg);
+        if (lsn > p.lper) issue_slices<LT>(p, lstage, ls0, lsn, 1, bar_lg);
+      }
+      // nothing for the walker to wait for but the read of ctx above
+      if (!p.pipelined && p.do_accept && blk != p.walker && !late_signal) atomicAdd(p.bar + 2, 1u);
+    }
+  }
+  // Warps 1..15: the last split's tree rows (its first chunk; this thread's
+  // first TP 16-byte pieces, converted when the chunk is built).
+  constexpr int kLoaders = kStepThreads - 32;
+  const int li = tid - 32;                       // loader index (< 0: warp 0)
+  constexpr int TP = 4;
+  const bool tree_split = unit >= 0 && split == p.splits - 1;
+  const int nt_all = min(kChunk, N);
+  const int tree_real = 2 * nt_all * (D / 8);     // 16-byte pieces with data
+  uint4 tv[TP];
+#pragma unroll
+  for (int u = 0; u < TP; ++u) {
+    const int it = li + u * kLoaders;
+    tv[u] = make_uint4(0u, 0u, 0u, 0u);
+    if (li >= 0 && tree_split && it < tree_real) {
+      const int ka = it / (D / 8), c = it % (D / 8);
+      const int kvi = ka >= nt_all ? 1 : 0, key = ka - kvi * nt_all;
+      tv[u] = __ldg(reinterpret_cast<const uint4*>(
+          (kvi ? p.tree_v : p.tree_k) + (static_cast<size_t>(key) * p.hkv + h) * D + c * 8));
+    }
   }
   if (unit >= 0 && warp == 2) {
     tc::tmem_alloc(s_tmem, kTmemCols);
@@ -758,22 +830,39 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       __syncwarp();
     }
   }
-  if (unit >= 0) {
-#pragma unroll
-    for (int u = 0; u < QU; ++u) {
-      const int it = tid + u * kStepThreads;
-      const int lr = it / (D / 8), c = it % (D / 8);
-      *reinterpret_cast<uint4*>(sQ + tc::sw128_offset(lr, c, kRowsPerTile)) = bf16x8_to_f16x8(qv[u]);
+  __syncthreads();   // barriers initialised, ctx known (unless pipelined)
+  if (!p.pipelined) {
+    C = s_C;
+    derive();
+  }
+  // ---- Q: once the bf16 rows have landed, warps 1..15 convert them into
+  // the fp16 swizzled tiles (the 128-row tile in sQ, the remainder rows in
+  // sQB); rows past the group's are zero
+  if (unit >= 0 && li >= 0) {
+    if (!wait_bounded([&]() { return mbar_try_wait(bar_q, 0); }) && li == 0)
+      report(p.status, DFV_DEV_TIMEOUT);
+    const uint8_t* qs = smem + L::kQStage;
+    constexpr int QA = kRowsPerTile * (D / 8);            // pieces of the 128-row tile
+    const int qall = QA + (ub ? p.nb * (D / 8) : 0);
+#pragma unroll 1
+    for (int it = li; it < qall; it += kLoaders) {
+      const int row = it / (D / 8), c = it % (D / 8);
+      const bool real = row < kRowsPerTile ? row < a_rows_g : row - kRowsPerTile < p.b_rows;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (real) {
+        const int srow = row < kRowsPerTile ? row : a_rows_g + (row - kRowsPerTile);
+        v = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(qs + static_cast<size_t>(srow) * D * 2 + c * 16));
+      }
+      if (row < kRowsPerTile) *reinterpret_cast<uint4*>(sQ + tc::sw128_offset(row, c, kRowsPerTile)) = v;
+      else *reinterpret_cast<uint4*>(sQB + tc::sw128_offset(row - kRowsPerTile, c, p.nb)) = v;
     }
   }
-  __syncthreads();   // barriers initialised, tree bookkeeping done, ctx known
-                     // (unless pipelined)
+  __syncthreads();   // Q converted, tree bookkeeping done
 
-  // ---- logits: CTAs without an attention unit scan their slices now (and
-  // so do the units when pipelined); slices beyond one per CTA (or unaligned
-  // rows) go through plain loads
-  auto accept_inputs = [&](bool units_too) {
-    if (lreg && (unit < 0 || units_too)) scan_slices<LT>(p, lstage, ls0, lsn, bar_lg, &s_ok);
+  // ---- logits: CTAs without an attention unit scan their staged slices;
+  // when nothing is staged, every CTA scans slices with plain loads
+  auto accept_inputs = [&]() {
+    if (lreg) scan_slices<LT>(p, lstage, ls0, lsn, bar_lg, &s_ok);
     if (!p.lbulk) plain_slices<LT>(p, blk, G);
     // ---- the walker keeps the tree's parents and tokens in smem
     if (blk == p.walker && tid < N) {
@@ -790,16 +879,12 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       const int nq = p.walker_local ? 1 : G;
       const int bq = p.walker_local ? 0 : blk;
       prequant_tree<D, FMT>(p, qdst, static_cast<int>(static_cast<long>(bq) * tot / nq),
-                       static_cast<int>(static_cast<long>(bq + 1) * tot / nq));
+                            static_cast<int>(static_cast<long>(bq + 1) * tot / nq));
     }
   };
-  if (!p.pipelined) {
-    C = s_C;
-    derive();
-  }
   // pipelined: this reads only the step's own inputs and workspace, and runs
   // while the previous kernel finishes; ctx and the K / V copy come after it
-  if (p.do_accept) accept_inputs(p.pipelined != 0);
+  if (p.do_accept) accept_inputs();
   if (p.pipelined) {
     grid_dep_wait();
     if (tid == 0) {
@@ -811,7 +896,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     derive();
   }
 
-  if (unit < 0 && late_signal) {
+  if (late_signal) {
     __syncthreads();   // every thread's partials and tree rows written
     signal_done();
   }
@@ -819,7 +904,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
   if (unit >= 0) {
     if (blk == 0 && tid < N && s_dep[tid] > p.max_depth) report(p.status, DFV_DEV_DEPTH);
     if (tid < kRowsPerTile) {
-      const int rg = mt * kRowsPerTile + tid;
+      const int rg = grp * kRowsPerTile + tid;
       if (rg < p.rows) {
         const int node = div_small(rg, p.group_m);
         s_row_node[tid] = node;
@@ -828,25 +913,40 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         s_row_node[tid] = -1;
         s_row_lo[tid] = 0x7fffffff;
       }
+    } else if (tid < kRowsPerTile + kMaxBRows) {
+      const int rb = tid - kRowsPerTile;
+      if (ub && rb < p.b_rows) {
+        const int node = div_small(p.n_grp * kRowsPerTile + rb, p.group_m);
+        s_brow_node[rb] = node;
+        s_brow_lo[rb] = p.window > 0 ? C + s_dep[node] - p.window + 1 : 0;
+      } else {
+        s_brow_node[rb] = -1;
+        s_brow_lo[rb] = 0x7fffffff;
+      }
     }
-    if (lreg && !p.pipelined) scan_slices<LT>(p, lstage, ls0, lsn, bar_lg, &s_ok);   // the staged logits slices first
-    else if (late_signal) __syncthreads();   // every thread's tree rows written
-    if (late_signal) signal_done();
     tc::fence_after_sync();
 
     const uint32_t tmem = *s_tmem;
-    const uint32_t t_s = tmem;              // S: columns [0, 128)
-    const uint32_t t_o = tmem + kChunk;     // O: columns [128, 128 + D)
+    const uint32_t t_s = tmem;                    // S: columns [0, 128)
+    const uint32_t t_o = tmem + kChunk;           // O: columns [128, 128 + D)
+    const uint32_t t_sb = tmem + kChunk + D;      // S_B^T: nb columns (rows), lanes = keys
+    const uint32_t t_ob = t_sb + (ub ? p.nb : 0); // O_B^T: D / 128 blocks of nb columns, lanes = dims
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int r = (warp & 3) * 32 + lane;   // this thread's row
-    const int hc = warp >> 2;               // its quarter of the keys / of O's columns
-    // A warp whose 32 rows all lie past the last row (the short tile) skips
+    const int r = (warp & 3) * 32 + lane;   // this thread's row (and key of S_B^T, dim of O_B^T)
+    const int hc = warp >> 2;               // its quarter of the keys / of O's columns / of B's rows
+    const int bcols = ub ? p.nb / 4 : 0;    // remainder rows this thread handles: [hc * bcols, +bcols)
+    // A warp whose 32 rows all lie past the last row (a padded tile) skips
     // the second half of the softmax and the epilogue: its P rows keep the
     // finite operand values under them, and its O rows reach no output.
-    auto rows_live = [&]() { return mt * kRowsPerTile + (warp & 3) * 32 < p.rows; };
-    uint32_t ph_kv = 0, ph_mma = 0;
+    const bool live = grp * kRowsPerTile + (warp & 3) * 32 < p.rows;
+    uint32_t ph_kv = 0, ph_mma = 0, ph_b = 0;
+    bool pend_b = false;   // the remainder rows' last O_B^T MMAs not waited for yet
     float m_run = -INFINITY, l_half = 0.f;
+    float mb[8], lb[8];   // remainder rows: running max, this key's share of the sums
+#pragma unroll
+    for (int c = 0; c < 8; ++c) { mb[c] = -INFINITY; lb[c] = 0.f; }
     bool o_valid = false, alive = true;
+    const float sc = p.scale_log2;
 
 #pragma unroll 1
     for (int i = 0; i < c1 - c0 && alive; ++i) {
@@ -861,6 +961,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         constexpr int PR = D / 8;                         // pieces per row
         const uint8_t* kb = p.k_cache + (static_cast<size_t>(h) * p.capacity + j0) * (D * 2);
         const uint8_t* vb = p.v_cache + (static_cast<size_t>(h) * p.capacity + j0) * (D * 2);
+#pragma unroll 1
         for (int it = tid; it < 2 * kChunk * PR; it += kStepThreads) {
           const int kvi = it / (kChunk * PR), rem = it % (kChunk * PR);
           const int key = rem / PR, c = rem % PR;
@@ -875,64 +976,66 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
           if (!cta_wait(bar_kv, ph_kv, &s_ok, p.status)) { alive = false; break; }
           ph_kv ^= 1u;
         }
-        // K: raw (sRawK or global) -> sK, V: raw (sK or global) -> sV, both
-        // [keys][D] swizzled, in one pass. A work item is a pair of Q4_0
-        // blocks (36 bytes = 9 words, 64 elements = one swizzle block) of
-        // one key row. Within a warp, lanes 8i..8i+7 take eight consecutive
-        // keys of the same pair: the 16-byte stores of each 8-lane phase
-        // then fall on 8 distinct swizzled granules, and the 9-word loads
-        // (word stride 9 * pairs-per-row between keys, 9 between pairs)
-        // fall on 32 distinct banks. Every raw word is loaded before the
-        // barrier, so V's raw rows in sK are consumed before K overwrites
-        // them.
+        // K: raw -> sK, V: raw -> sV, both [keys][D] swizzled. A work item is
+        // a pair of Q4_0 blocks (36 bytes = 9 words, 64 elements = one
+        // swizzle block) of one key row. Within a warp, lanes 8i..8i+7 take
+        // eight consecutive keys of the same pair: the 16-byte stores of each
+        // 8-lane phase then fall on 8 distinct swizzled granules, and the
+        // 9-word loads (word stride 9 * pairs-per-row between keys, 9 between
+        // pairs) fall on 32 distinct banks. Every raw word (staged in sV) is
+        // loaded before the barrier, so the raw rows are consumed before V^
+        // overwrites them; the decode is one loop body for both items.
         {
           constexpr int PPK = D / 64;                     // block pairs per key row
           constexpr int HALF = kChunk * PPK;              // items per operand
           constexpr int IPT = (2 * HALF + kStepThreads - 1) / kStepThreads;
-          uint32_t w[IPT][9];
-#pragma unroll
-          for (int u = 0; u < IPT; ++u) {
+          static_assert(IPT <= 2, "at most two dequant items per thread");
+          auto item = [&](int u, int& kvi, int& key, int& pp) {
             const int g = tid + u * kStepThreads;
-            const int kvi = g / HALF, rem = g % HALF;
-            const int l = rem & 31;
-            const int key = (rem >> 5) * (32 / PPK) + (l & 7) + 8 * (l / (8 * PPK));
-            const int pp = (l >> 3) % PPK;
-            const bool live = g < 2 * HALF && key < nk;
+            kvi = g / HALF;
+            const int rem = g % HALF, l = rem & 31;
+            key = (rem >> 5) * (32 / PPK) + (l & 7) + 8 * (l / (8 * PPK));
+            pp = (l >> 3) % PPK;
+            return g < 2 * HALF;
+          };
+          uint32_t w0[9], w1[9];
+          auto load = [&](int u, uint32_t* w) {
+            int kvi, key, pp;
+            const bool on = item(u, kvi, key, pp) && key < nk;
             const uint8_t* base;
-            if constexpr (L::kBulk) base = kvi ? sK : sRawK;
+            if constexpr (L::kBulk) base = sV + (kvi ? L::kRawV : L::kRawK);
             else base = (kvi ? p.v_cache : p.k_cache) + (static_cast<size_t>(h) * p.capacity + j0) * L::kRowB;
-            const uint32_t* src = reinterpret_cast<const uint32_t*>(base + (live ? key * L::kRowB + pp * 36 : 0));
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(base + (on ? key * L::kRowB + pp * 36 : 0));
 #pragma unroll
-            for (int e = 0; e < 9; ++e) w[u][e] = live ? src[e] : 0u;
-          }
-          if constexpr (L::kBulk) __syncthreads();   // raw V (in sK) consumed
-#pragma unroll
+            for (int e = 0; e < 9; ++e) w[e] = on ? src[e] : 0u;
+          };
+          load(0, w0);
+          if (IPT > 1) load(1, w1);
+          if constexpr (L::kBulk) __syncthreads();   // raw rows (in sV) consumed
+#pragma unroll 1
           for (int u = 0; u < IPT; ++u) {
-            const int g = tid + u * kStepThreads;
-            if (g < 2 * HALF) {
-              const int kvi = g / HALF, rem = g % HALF;
-              const int l = rem & 31;
-              const int key = (rem >> 5) * (32 / PPK) + (l & 7) + 8 * (l / (8 * PPK));
-              const int pp = (l >> 3) % PPK;
+            int kvi, key, pp;
+            if (item(u, kvi, key, pp)) {
               uint4 o4[8];
-              q4_0_pair_chunks(w[u], o4);       // all-zero blocks dequantise to zeros
+              q4_0_pair_chunks(w0, o4);       // all-zero blocks dequantise to zeros
               uint8_t* dst = kvi ? sV : sK;
 #pragma unroll
               for (int e = 0; e < 8; ++e)
                 *reinterpret_cast<uint4*>(dst + tc::sw128_offset(key, pp * 8 + e, kChunk)) = o4[e];
             }
+#pragma unroll
+            for (int e = 0; e < 9; ++e) w0[e] = w1[e];
           }
         }
       } else {
         // tree chunk: keys t = 0..N-1 from tree_k / tree_v (bf16 -> fp16);
-        // the other key rows are zero. The first TP pieces of each thread
-        // were loaded at entry.
+        // the other key rows are zero. The first TP pieces of each loader
+        // thread were loaded at entry.
         const int nt = nt_all;
         const int real = tree_real;
         if (kQ4 && p.tree_q) {
           // the tree rows as the commit stores them: each 32-value block is
           // quantised to Q4_0 (the commit's rule) and dequantised again
-          constexpr int NB = D / 32;
 #pragma unroll 1
           for (int it = tid; it < 2 * nt * NB; it += kStepThreads) {
             const int ka = it / NB, b = it % NB;
@@ -959,10 +1062,10 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
             for (int e = 0; e < 4; ++e)
               *reinterpret_cast<uint4*>((kvi ? sV : sK) + tc::sw128_offset(key, b * 4 + e, kChunk)) = o4[e];
           }
-        } else {
+        } else if (li >= 0) {
 #pragma unroll
           for (int u = 0; u < TP; ++u) {
-            const int it = tid + u * kStepThreads;
+            const int it = li + u * kLoaders;
             if (it < real) {
               const int ka = it / (D / 8), c = it % (D / 8);
               const int kvi = ka >= nt ? 1 : 0, key = ka - kvi * nt;
@@ -971,7 +1074,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
             }
           }
 #pragma unroll 1
-          for (int it = tid + TP * kStepThreads; it < real; it += kStepThreads) {
+          for (int it = li + TP * kLoaders; it < real; it += kLoaders) {
             const int ka = it / (D / 8), c = it % (D / 8);
             const int kvi = ka >= nt ? 1 : 0, key = ka - kvi * nt;
             const uint4 v = __ldg(reinterpret_cast<const uint4*>(
@@ -981,6 +1084,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
           }
         }
         const int zero = 2 * (kChunk - nt) * (D / 8);
+#pragma unroll 1
         for (int it = tid; it < zero; it += kStepThreads) {
           const int ka = it / (D / 8), c = it % (D / 8);
           const int kvi = ka >= kChunk - nt ? 1 : 0, key = nt + ka - kvi * (kChunk - nt);
@@ -991,30 +1095,44 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       fence_proxy_async_smem();
       __syncthreads();
 
-      // ---- S = Q K^T (M = 128 rows, N = 128 keys, K = D)
+      // ---- S = Q K^T (M = 128 rows, N = 128 keys, K = D), committed on its
+      // own; then, for the remainder rows, S_B^T = K Q_B^T (M = 128 keys,
+      // N = nb rows, K = D), which runs under the tile's softmax
       if (tid == 0) {
         tc::fence_after_sync();
-        const uint32_t idesc = tc::idesc_f16(kRowsPerTile, kChunk);
-#pragma unroll
+        const uint32_t ida = tc::idesc_f16(kRowsPerTile, kChunk);
+        const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK), qb = smem_u32(sQB);
+#pragma unroll 1
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = static_cast<uint32_t>((kk >> 2) * kRowsPerTile * 128 + (kk & 3) * 32);
-          tc::mma_f16(t_s, tc::smem_desc_sw128(smem_u32(sQ) + off, 1024),
-                      tc::smem_desc_sw128(smem_u32(sK) + off, 1024), idesc, kk > 0 ? 1u : 0u);
+          tc::mma_f16(t_s, tc::smem_desc_sw128(qa + off, 1024), tc::smem_desc_sw128(ka + off, 1024), ida,
+                      kk > 0 ? 1u : 0u);
         }
         tc::commit(bar_mma);
+        if (ub) {
+          const uint32_t idb = tc::idesc_f16(kChunk, p.nb);
+#pragma unroll 1
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = static_cast<uint32_t>((kk >> 2) * kChunk * 128 + (kk & 3) * 32);
+            const uint32_t offb = static_cast<uint32_t>((kk >> 2) * p.nb * 128 + (kk & 3) * 32);
+            tc::mma_f16(t_sb, tc::smem_desc_sw128(ka + off, 1024), tc::smem_desc_sw128(qb + offb, 1024),
+                        idb, kk > 0 ? 1u : 0u);
+          }
+          tc::commit(bar_mmab);
+        }
       }
       if (!cta_wait(bar_mma, ph_mma, &s_ok, p.status)) { alive = false; break; }
       ph_mma ^= 1u;
       tc::fence_after_sync();
 
-      // ---- masked softmax: four threads per row, 32 keys each
+      // ---- masked softmax of the 128-row tile: four threads per row, 32
+      // keys each, loaded from TMEM once
       {
         const int kb0 = hc * 32;
         float s[32];
         tc::ld32(t_s + lane_base + kb0, s);
         const int node = s_row_node[r], lo = s_row_lo[r];
         float cm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        const float sc = p.scale_log2;
         if (committed) {
           // visible keys of this row form the range [kmin, kmax)
           const int kmin = min(max(lo - j0, 0), kChunk) - kb0;
@@ -1037,166 +1155,317 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
           }
         }
         s_pmax[hc][r] = fmaxf(fmaxf(cm[0], cm[1]), fmaxf(cm[2], cm[3]));
-        __syncthreads();
-        if (rows_live()) {
-        const float cmax = fmaxf(fmaxf(s_pmax[0][r], s_pmax[1][r]), fmaxf(s_pmax[2][r], s_pmax[3][r]));
-        float alpha = 1.f;
-        bool rescale = false;
-        if (m_run == -INFINITY) {
-          m_run = cmax;                       // O and l are still zero
-        } else if (cmax > m_run + kRescaleLog2) {
-          alpha = tc::ex2(m_run - cmax);
-          rescale = true;
-          m_run = cmax;
+        if (ub) {
+          // S_B^T reads K^ in sK, which P overwrites below: its commit ends
+          // the barrier of the maxima
+          if (!cta_wait(bar_mmab, ph_b, &s_ok, p.status)) { alive = false; break; }
+          ph_b ^= 1u;
+        } else {
+          __syncthreads();
         }
-        const float sub = m_run == -INFINITY ? 0.f : m_run;
-        float rs4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t w4[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float p0 = tc::ex2(s[c * 8 + 2 * e] - sub);
-            const float p1 = tc::ex2(s[c * 8 + 2 * e + 1] - sub);
-            rs4[e] += p0 + p1;
-            w4[e] = pack_half2(p0, p1);
+        if (live) {
+          const float cmax = fmaxf(fmaxf(s_pmax[0][r], s_pmax[1][r]), fmaxf(s_pmax[2][r], s_pmax[3][r]));
+          float alpha = 1.f;
+          bool rescale = false;
+          if (m_run == -INFINITY) {
+            m_run = cmax;                       // O and l are still zero
+          } else if (cmax > m_run + kRescaleLog2) {
+            alpha = tc::ex2(m_run - cmax);
+            rescale = true;
+            m_run = cmax;
           }
-          *reinterpret_cast<uint4*>(sK + tc::sw128_offset(r, hc * 4 + c, kRowsPerTile)) =
-              make_uint4(w4[0], w4[1], w4[2], w4[3]);
-        }
-        l_half = l_half * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
-        if (o_valid && __any_sync(0xffffffffu, rescale)) {
-          // this warp's quarter of the row's O columns
-          constexpr int CW = D / 4 < 32 ? D / 4 : 32;
+          const float sub = m_run == -INFINITY ? 0.f : m_run;
+          float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float p0 = tc::ex2(s[c * 8 + 2 * e] - sub);
+              const float p1 = tc::ex2(s[c * 8 + 2 * e + 1] - sub);
+              rs4[e] += p0 + p1;
+              w4[e] = pack_half2(p0, p1);
+            }
+            *reinterpret_cast<uint4*>(sK + tc::sw128_offset(r, hc * 4 + c, kRowsPerTile)) =
+                make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+          l_half = l_half * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
+          if (o_valid && __any_sync(0xffffffffu, rescale)) {
+            // this warp's quarter of the row's O columns
 #pragma unroll 1
-          for (int c = 0; c < (D / 4) / CW; ++c) {
-            const uint32_t col = static_cast<uint32_t>(hc * (D / 4) + c * CW);
-            float ov[32];
-            if constexpr (CW == 32) tc::ld32(t_o + lane_base + col, ov);
-            else tc::ld16(t_o + lane_base + col, ov);
+            for (int b = 0; b < D / 32; ++b) {
+              const uint32_t col = static_cast<uint32_t>(hc * (D / 4) + b * 8);
+              float ov[8];
+              tc::ld8(t_o + lane_base + col, ov);
 #pragma unroll
-            for (int e = 0; e < CW; ++e) ov[e] *= alpha;
-            if constexpr (CW == 32) tc::st32(t_o + lane_base + col, ov);
-            else tc::st16(t_o + lane_base + col, ov);
+              for (int e = 0; e < 8; ++e) ov[e] *= alpha;
+              tc::st8(t_o + lane_base + col, ov);
+            }
           }
-        }
         }
       }
       fence_proxy_async_smem();
       tc::fence_before_sync();
       __syncthreads();
 
-      // ---- O += P V (M = 128 rows, N = D, K = 128 keys; V MN-major)
+      // ---- O += P V (M = 128 rows, N = D, K = 128 keys; V MN-major); it runs
+      // under the remainder rows' softmax
       if (tid == 0) {
         tc::fence_after_sync();
-        const uint32_t idesc = tc::idesc_f16(kRowsPerTile, D, true);
-#pragma unroll
+        const uint32_t ida = tc::idesc_f16(kRowsPerTile, D, true);
+        const uint32_t pa = smem_u32(sK), va = smem_u32(sV);
+#pragma unroll 1
         for (int kk = 0; kk < kChunk / 16; ++kk) {
           const uint32_t offa = static_cast<uint32_t>((kk >> 2) * kRowsPerTile * 128 + (kk & 3) * 32);
-          const uint32_t offb = static_cast<uint32_t>(kk * 16 * 128);
-          tc::mma_f16(t_o, tc::smem_desc_sw128(smem_u32(sK) + offa, 1024),
-                      tc::smem_desc_sw128_mn(smem_u32(sV) + offb, kChunk * 128, 1024), idesc,
+          const uint32_t offv = static_cast<uint32_t>(kk * 16 * 128);
+          tc::mma_f16(t_o, tc::smem_desc_sw128(pa + offa, 1024),
+                      tc::smem_desc_sw128_mn(va + offv, kChunk * 128, 1024), ida,
                       (o_valid || kk > 0) ? 1u : 0u);
         }
         tc::commit(bar_mma);
       }
+
+      // ---- the remainder rows (S_B^T: lanes = keys): one thread per key and
+      // bcols rows, their running max and this key's share of their sums in
+      // registers (every thread of a row computes the same max from the same
+      // partial maxima); then O_B^T += V^T P_B^T (M = 128 dims per block,
+      // N = nb, K = 128 keys; V^T is sV read as an MN-major A operand)
+      if constexpr (L::kHasB) {
+        if (ub) {
+          tc::fence_after_sync();
+          float sb[8];
+          if (bcols == 8) tc::ld8(t_sb + lane_base + hc * 8, sb);
+          else tc::ld4(t_sb + lane_base + hc * 4, sb);
+          const int key = r;   // lane r of S_B^T is key r of the chunk
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            if (c < bcols) {
+              const int rb = hc * bcols + c;
+              const int bn = s_brow_node[rb];
+              bool vis;
+              if (committed) vis = bn >= 0 && key < nk && j0 + key >= s_brow_lo[rb];
+              else vis = bn >= 0 && key < kMaskWords * 32 && ((s_anc[bn][key >> 5] >> (key & 31)) & 1u);
+              const float x = vis ? sb[c] * sc : -INFINITY;
+              sb[c] = x;
+              float mx = x;
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+              if (lane == 0) s_bmax[warp & 3][rb] = mx;
+            }
+          }
+          __syncthreads();
+          float ab[8];
+          bool bres = false;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            ab[c] = 1.f;
+            if (c < bcols) {
+              const int rb = hc * bcols + c;
+              const float cmax = fmaxf(fmaxf(s_bmax[0][rb], s_bmax[1][rb]), fmaxf(s_bmax[2][rb], s_bmax[3][rb]));
+              if (mb[c] == -INFINITY) {
+                mb[c] = cmax;
+              } else if (cmax > mb[c] + kRescaleLog2) {
+                ab[c] = tc::ex2(mb[c] - cmax);
+                bres = true;
+                mb[c] = cmax;
+              }
+              const float pv = tc::ex2(sb[c] - (mb[c] == -INFINITY ? 0.f : mb[c]));
+              lb[c] = lb[c] * ab[c] + pv;
+              // P_B: K-major [nb rows][128 keys] past P in sK
+              *reinterpret_cast<__half*>(sK + L::kPB + tc::sw128_offset(rb, r >> 3, p.nb) + (r & 7) * 2) =
+                  __float2half_rn(pv);
+            }
+          }
+          if (o_valid && __any_sync(0xffffffffu, bres)) {
+            // O_B^T lanes are head dims: this thread's dim r of every 128-dim
+            // block, columns = its remainder rows
+#pragma unroll 1
+            for (int m2 = 0; m2 < D / 128; ++m2) {
+              const uint32_t col = static_cast<uint32_t>(m2 * p.nb + hc * bcols);
+              float ov[8];
+              if (bcols == 8) tc::ld8(t_ob + lane_base + col, ov);
+              else tc::ld4(t_ob + lane_base + col, ov);
+#pragma unroll
+              for (int c = 0; c < 8; ++c) ov[c] *= ab[c];
+              if (bcols == 8) tc::st8(t_ob + lane_base + col, ov);
+              else tc::st4(t_ob + lane_base + col, ov);
+            }
+          }
+          fence_proxy_async_smem();
+          tc::fence_before_sync();
+          __syncthreads();
+          if (tid == 0) {
+            tc::fence_after_sync();
+            const uint32_t idb = tc::idesc_f16(kRowsPerTile, p.nb, false, true);
+            const uint32_t va = smem_u32(sV), pb = smem_u32(sK) + L::kPB;
+#pragma unroll 1
+            for (int kk = 0; kk < kChunk / 16; ++kk) {
+              const uint32_t offv = static_cast<uint32_t>(kk * 16 * 128);
+              const uint32_t offb = static_cast<uint32_t>((kk >> 2) * p.nb * 128 + (kk & 3) * 32);
+#pragma unroll
+              for (int m2 = 0; m2 < D / 128; ++m2)
+                tc::mma_f16(t_ob + m2 * p.nb,
+                            tc::smem_desc_sw128_mn(va + m2 * 2 * kChunk * 128 + offv, kChunk * 128, 1024),
+                            tc::smem_desc_sw128(pb + offb, 1024), idb, (o_valid || kk > 0) ? 1u : 0u);
+            }
+            tc::commit(bar_mmab);
+          }
+          pend_b = true;
+        }
+      }
       if (!cta_wait(bar_mma, ph_mma, &s_ok, p.status)) { alive = false; break; }
       ph_mma ^= 1u;
+      // the next chunk overwrites sK / sV: the remainder rows' MMAs too must
+      // be done (the last chunk's are waited for after the tile's epilogue)
+      if (pend_b && i + 1 < c1 - c0) {
+        if (!cta_wait(bar_mmab, ph_b, &s_ok, p.status)) { alive = false; break; }
+        ph_b ^= 1u;
+        pend_b = false;
+      }
       o_valid = true;
       tc::fence_after_sync();
     }
 
-    // ---- epilogue: O rows from TMEM -> workspace (or the output when
-    // there is one split)
+    // ---- epilogue: normalised O rows from TMEM (each thread's columns in
+    // one batch of loads) -> the unit's partial rows staged in smem (D fp16
+    // values, then the row's (max, sum), 16 bytes more per row) -> one bulk
+    // copy to the workspace; or straight to the output (fp32) when there is
+    // one split
     s_l[hc][r] = l_half;
-    if (hc == 0) s_m[r] = m_run;
-    __syncthreads();
-    {
-      // Each warp owns 32 rows (its TMEM lane quadrant) and a quarter of the
-      // D columns, moved in CW-column blocks through smem so that global
-      // stores are row-contiguous. The 16 warps' staging areas (at most
-      // 16 x 32 x 36 floats) run from sQ over sK into sV, all free once the
-      // last MMA has completed.
-      constexpr int CW = D / 4 < 32 ? D / 4 : 32;   // columns per block
-      constexpr int LPR = CW / 4;                    // lanes per row (float4 each)
-      constexpr int RPI = 32 / LPR;                  // rows per store instruction
-      constexpr int NI = 32 / RPI;                   // store instructions per block
-      constexpr int SS = CW + 4;                     // staging row stride (floats)
-      static_assert((kStepThreads / 32) * 32 * SS * 4 <= L::kRawK, "staging overruns sV");
-      float* stage = reinterpret_cast<float*>(sQ) + warp * (32 * SS);
-      float inv[NI];
+    if constexpr (L::kHasB) {
+      if (ub) {
+        // the remainder rows' sums over this warp's 32 keys, then (below)
+        // over the four lane quadrants
 #pragma unroll
-      for (int i = 0; i < NI; ++i) {
-        const int row = (warp & 3) * 32 + i * RPI + lane / LPR;
-        const float l = (s_l[0][row] + s_l[1][row]) + (s_l[2][row] + s_l[3][row]);
-        inv[i] = l > 0.f ? __fdividef(1.f, l) : 0.f;
-      }
-#pragma unroll 1
-      for (int c = 0; c < (rows_live() ? (D / 4) / CW : 0); ++c) {
-        const int col = hc * (D / 4) + c * CW;
-        float ov[32];
-        if constexpr (CW == 32) tc::ld32(t_o + lane_base + col, ov);
-        else tc::ld16(t_o + lane_base + col, ov);
+        for (int c = 0; c < 8; ++c) {
+          if (c < bcols) {
+            float v = lb[c];
 #pragma unroll
-        for (int e = 0; e < CW; e += 4)
-          *reinterpret_cast<float4*>(stage + lane * SS + e) = make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
-        __syncwarp();
-        float4 v[NI];
-#pragma unroll
-        for (int i = 0; i < NI; ++i) {
-          const int rr = i * RPI + lane / LPR;            // row within the warp's 32
-          v[i] = *reinterpret_cast<const float4*>(stage + rr * SS + (lane % LPR) * 4);
-        }
-#pragma unroll
-        for (int i = 0; i < NI; ++i) {
-          const int rr = i * RPI + lane / LPR;
-          const int row = (warp & 3) * 32 + rr;
-          const int rg = mt * kRowsPerTile + row;
-          if (rg < p.rows && o_valid && alive && inv[i] > 0.f) {
-            float4 w = v[i];
-            w.x *= inv[i]; w.y *= inv[i]; w.z *= inv[i]; w.w *= inv[i];
-            const int cc4 = col + (lane % LPR) * 4;
-            if (p.splits == 1) {
-              const int node = div_small(rg, p.group_m), qh = h * p.group + rg - node * p.group;
-              *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(node) * p.hq + qh) * D + cc4) = w;
-            } else {
-              __half2 h01 = __floats2half2_rn(w.x, w.y), h23 = __floats2half2_rn(w.z, w.w);
-              uint2 hv;
-              hv.x = *reinterpret_cast<uint32_t*>(&h01);
-              hv.y = *reinterpret_cast<uint32_t*>(&h23);
-              *reinterpret_cast<uint2*>(p.part_o + (static_cast<size_t>(unit) * kRowsPerTile + row) * D + cc4) = hv;
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0) {
+              s_bl[warp & 3][hc * bcols + c] = v;
+              if ((warp & 3) == 0) s_bm[hc * bcols + c] = mb[c];
             }
           }
         }
-        __syncwarp();
       }
-      const int rg = mt * kRowsPerTile + r;
-      if (hc == 0 && rg < p.rows) {
-        const float m = s_m[r];
-        const float l = (s_l[0][r] + s_l[1][r]) + (s_l[2][r] + s_l[3][r]);
-        const bool ok = o_valid && alive && l > 0.f;
+    }
+    __syncthreads();
+    bool ok_all = o_valid && alive;
+    constexpr int RB = kPartRowBytes<D>;   // bytes of one partial row
+    uint8_t* stage = smem;                 // [rows_g][RB], over sQ and sK (free after the last MMA)
+    if (ok_all && live) {
+      // the TMEM loads are warp-wide (.sync.aligned): every lane loads, the
+      // lanes of real rows store
+      const bool mine = r < a_rows_g;
+      const float l = (s_l[0][r] + s_l[1][r]) + (s_l[2][r] + s_l[3][r]);
+      const float inv = l > 0.f ? __fdividef(1.f, l) : 0.f;
+      constexpr int CT = D / 4;            // columns of this thread
+      float ov[CT];
+      const uint32_t col0 = t_o + lane_base + hc * CT;
+      if constexpr (CT == 64) tc::ld32x2(col0, col0 + 32, ov);
+      else if constexpr (CT == 32) tc::ld32(col0, ov);
+      else tc::ld16(col0, ov);
+      if (mine) {
+        const int rg = grp * kRowsPerTile + r;
+        const int node = div_small(rg, p.group_m), qh = h * p.group + rg - node * p.group;
         if (p.splits == 1) {
-          const int node = div_small(rg, p.group_m), qh = h * p.group + rg - node * p.group;
-          if (p.lse != nullptr) p.lse[node * p.hq + qh] = (m + log2f(l)) * 0.69314718055994531f;
+          float4* dst = reinterpret_cast<float4*>(p.out + (static_cast<size_t>(node) * p.hq + qh) * D + hc * CT);
+#pragma unroll
+          for (int e = 0; e < CT / 4; ++e)
+            dst[e] = make_float4(ov[4 * e] * inv, ov[4 * e + 1] * inv, ov[4 * e + 2] * inv, ov[4 * e + 3] * inv);
+          if (hc == 0 && p.lse != nullptr) p.lse[node * p.hq + qh] = (m_run + log2f(l)) * 0.69314718055994531f;
         } else {
-          p.part_ml[static_cast<size_t>(unit) * kRowsPerTile + r] =
-              make_float2(ok ? m : -INFINITY, ok ? l : 0.f);
+          uint4* dst = reinterpret_cast<uint4*>(stage + r * RB + hc * CT * 2);
+#pragma unroll
+          for (int e = 0; e < CT / 8; ++e)
+            dst[e] = make_uint4(pack_half2(ov[8 * e] * inv, ov[8 * e + 1] * inv),
+                                pack_half2(ov[8 * e + 2] * inv, ov[8 * e + 3] * inv),
+                                pack_half2(ov[8 * e + 4] * inv, ov[8 * e + 5] * inv),
+                                pack_half2(ov[8 * e + 6] * inv, ov[8 * e + 7] * inv));
+          if (hc == 0)
+            *reinterpret_cast<float2*>(stage + r * RB + D * 2) = make_float2(l > 0.f ? m_run : -INFINITY, l);
+        }
+      }
+    }
+    if (pend_b) {
+      // the remainder rows' last O_B^T MMAs, which ran under the tile's
+      // epilogue (waited for even after a timeout: TMEM is freed below)
+      if (!cta_wait(bar_mmab, ph_b, &s_ok, p.status)) ok_all = false;
+      ph_b ^= 1u;
+      pend_b = false;
+      tc::fence_after_sync();
+    }
+    if constexpr (L::kHasB) {
+      if (ub && ok_all) {
+        // O_B^T: lane = dim r of each 128-dim block, columns = remainder
+        // rows; both blocks in one batch of loads
+        float ov[16];
+        const uint32_t col0 = t_ob + lane_base + hc * bcols;
+        if constexpr (D / 128 == 2) {
+          if (bcols == 8) tc::ld8x2(col0, col0 + p.nb, ov);
+          else tc::ld4x2(col0, col0 + p.nb, ov);
+        } else {
+          if (bcols == 8) tc::ld8(col0, ov);
+          else tc::ld4(col0, ov);
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int rb = hc * bcols + c;
+          if (c < bcols && rb < p.b_rows) {
+            const float l = (s_bl[0][rb] + s_bl[1][rb]) + (s_bl[2][rb] + s_bl[3][rb]);
+            const float inv = l > 0.f ? __fdividef(1.f, l) : 0.f;
+            const int row = kRowsPerTile + rb;
+            const int rg = p.n_grp * kRowsPerTile + rb;
+            const int node = div_small(rg, p.group_m), qh = h * p.group + rg - node * p.group;
+#pragma unroll
+            for (int m2 = 0; m2 < D / 128; ++m2) {
+              const int d = m2 * 128 + r;
+              const float v = (bcols == 8 ? ov[m2 * 8 + c] : ov[(m2 * 4 + c) & 15]) * inv;
+              if (p.splits == 1) p.out[(static_cast<size_t>(node) * p.hq + qh) * D + d] = v;
+              else *reinterpret_cast<__half*>(stage + row * RB + d * 2) = __float2half_rn(v);
+            }
+            if (lane == 0 && (warp & 3) == 0) {
+              if (p.splits == 1) {
+                if (p.lse != nullptr) p.lse[node * p.hq + qh] = (s_bm[rb] + log2f(l)) * 0.69314718055994531f;
+              } else {
+                *reinterpret_cast<float2*>(stage + row * RB + D * 2) =
+                    make_float2(l > 0.f ? s_bm[rb] : -INFINITY, l);
+              }
+            }
+          }
         }
       }
     }
     tc::fence_before_sync();
+    fence_proxy_async_smem();   // the staged rows, before the bulk copy reads them
     __syncthreads();
-    if (tid == 0 && p.splits > 1) {
-      // The split group's word: each CTA adds 1 (low 16 bits: arrivals;
-      // high 16 bits: a generation); the last to arrive adds 2^16 - n, which
-      // clears the count and advances the generation for the next launch.
-      // Every CTA of the group reads the same generation g from its own add
-      // and marks its partial written with (g + 1) mod 2^16.
-      const unsigned int n = static_cast<unsigned int>(p.splits);
-      if ((arrive_old & 0xFFFFu) == n - 1) atomicAdd(p.bar + 4 + 2 * (unit / p.splits), 0x10000u - n);
-      s_tag = ((arrive_old >> 16) + 1u) & 0xFFFFu;
-      __threadfence();   // the CTA's partial rows before its ready word
-      asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p.ready + unit), "r"(s_tag) : "memory");
+    if (p.splits > 1) {
+      uint8_t* part = p.part + static_cast<size_t>(unit) * kMaxGroupRows * RB;
+      if (!ok_all) {
+        // a timed-out unit publishes empty rows (max -inf, sum 0): the merge
+        // leaves it out (the status reports the timeout)
+        if (tid < rows_g)
+          *reinterpret_cast<float2*>(part + tid * RB + D * 2) = make_float2(-INFINITY, 0.f);
+        __syncthreads();
+      }
+      if (tid == 0) {
+        if (ok_all) {
+          bulk_s2g(part, stage, static_cast<uint32_t>(rows_g * RB));
+          bulk_commit_wait();
+        }
+        // The split group's word: each CTA adds 1 (low 16 bits: arrivals;
+        // high 16 bits: a generation); the last to arrive adds 2^16 - n,
+        // which clears the count and advances the generation for the next
+        // launch. Every CTA of the group reads the same generation g from its
+        // own add and marks its partial written with (g + 1) mod 2^16.
+        const unsigned int n = static_cast<unsigned int>(p.splits);
+        if ((arrive_old & 0xFFFFu) == n - 1) atomicAdd(p.bar + 4 + 2 * (unit / p.splits), 0x10000u - n);
+        s_tag = ((arrive_old >> 16) + 1u) & 0xFFFFu;
+        fence_proxy_async_global();   // the bulk writes, before the generic release below
+        __threadfence();              // the CTA's partial rows before its ready word
+        asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p.ready + unit), "r"(s_tag) : "memory");
+      }
     }
     if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
   }
@@ -1206,57 +1475,53 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
   if (p.do_accept && blk == p.walker) walker_tail<D, FMT>(p, G, C, s_ctx_ok != 0, sQ, sK, s_wpar, s_wtok);
 
   // ================================================================ merge
-  // Each of the `splits` CTAs of a (KV head, row tile) group waits for the
+  // Each of the `splits` CTAs of a (KV head, tile group) group waits for the
   // group's partials to be marked ready, then merges its share of the
-  // group's rows over the splits by log-sum-exp. A thread's first fp16 partials are loaded first; the
-  // (m, l) pairs of the CTA's rows go through smem, where one warp per row
-  // turns them into normalised weights.
+  // group's rows over the splits by log-sum-exp: the rows (values, max and
+  // sum) of every split's partial arrive by one bulk copy per split into
+  // smem; one warp per row turns the (max, sum) pairs into weights.
   if (unit >= 0 && p.splits > 1) {
-    const int grp = unit / p.splits, split = unit % p.splits;
+    constexpr int RB = kPartRowBytes<D>;
+    const int gi = unit / p.splits, split_ = unit % p.splits;
     if (warp == 0) {
       __syncwarp();   // s_tag was written by lane 0
-      const bool ok = wait_ready(p.ready + static_cast<size_t>(grp) * p.splits, p.splits, s_tag);
+      const bool ok = wait_ready(p.ready + static_cast<size_t>(gi) * p.splits, p.splits, s_tag);
       if (!ok && lane == 0) report(p.status, DFV_DEV_TIMEOUT);
       if (lane == 0) s_ok = ok ? 1 : 0;
     }
     __syncthreads();
     if (!s_ok) return;
-    const int h_ = grp / p.n_mt, mt_ = grp % p.n_mt;
-    const int rows_t = min(kRowsPerTile, p.rows - mt_ * kRowsPerTile);
-    const int r0 = split * rows_t / p.splits, r1 = (split + 1) * rows_t / p.splits;
+    const int h_ = gi / p.n_grp, g_ = gi % p.n_grp;
+    const bool ub_ = p.has_b && g_ == p.n_grp - 1;
+    const int rows_t = min(kRowsPerTile, p.rows - g_ * kRowsPerTile) + (ub_ ? p.b_rows : 0);
+    const int r0 = split_ * rows_t / p.splits, r1 = (split_ + 1) * rows_t / p.splits;
     const int nr = r1 - r0, S = p.splits;
-    const size_t ubase = static_cast<size_t>(grp) * S;
-    constexpr int SB = 20;          // partials of one item in flight at once
-    constexpr int DV = D / 4;       // 4-column items per row
-    const int items = nr * DV;
-    auto load_batch = [&](int it, int s0, uint2* ov) {
-      const int rr = r0 + it / DV, d = (it % DV) * 4;
-#pragma unroll
-      for (int u = 0; u < SB; ++u) {
-        ov[u] = make_uint2(0u, 0u);
-        if (it < items && s0 + u < S)
-          ov[u] = __ldcg(reinterpret_cast<const uint2*>(
-              p.part_o + ((ubase + s0 + u) * kRowsPerTile + rr) * D + d));
-      }
-    };
-    uint2 ov[SB];
-    load_batch(tid, 0, ov);
-    float2* s_ml = reinterpret_cast<float2*>(sQ);              // [nr][S]
-    float* s_w = reinterpret_cast<float*>(s_ml + nr * S);      // [nr][S]
-    for (int i = tid; i < nr * S; i += kStepThreads) {
-      const int rr = i / S, sp = i % S;
-      s_ml[i] = __ldcg(&p.part_ml[(ubase + sp) * kRowsPerTile + r0 + rr]);
+    if (nr <= 0) return;
+    const size_t ubase = static_cast<size_t>(gi) * S;
+    uint8_t* mst = sK;   // [S][nr][RB]
+    if (tid == 0) {
+      fence_proxy_async_global();   // the acquired partials, before the async-proxy reads
+      mbar_arrive_expect_tx(bar_q, static_cast<uint32_t>(S * nr * RB));
+      for (int s = 0; s < S; ++s)
+        bulk_g2s(mst + static_cast<size_t>(s) * nr * RB, p.part + ((ubase + s) * kMaxGroupRows + r0) * RB,
+                 static_cast<uint32_t>(nr * RB), bar_q);
     }
-    __syncthreads();
+    if (!wait_bounded([&]() { return mbar_try_wait(bar_q, 1); })) {
+      if (tid == 0) report(p.status, DFV_DEV_TIMEOUT);
+      return;
+    }
+    float* s_w = reinterpret_cast<float*>(sQ);      // [nr][S] normalised weights
+#pragma unroll 1
     for (int rr = warp; rr < nr; rr += kStepThreads / 32) {
+      auto ml = [&](int sp) { return *reinterpret_cast<const float2*>(mst + (static_cast<size_t>(sp) * nr + rr) * RB + D * 2); };
       float M = -INFINITY;
-      for (int sp = lane; sp < S; sp += 32) M = fmaxf(M, s_ml[rr * S + sp].x);
+      for (int sp = lane; sp < S; sp += 32) M = fmaxf(M, ml(sp).x);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
       float lsum = 0.f;
       for (int sp = lane; sp < S; sp += 32) {
-        const float2 ml = s_ml[rr * S + sp];
-        const float w = ml.x == -INFINITY ? 0.f : tc::ex2(ml.x - M) * ml.y;
+        const float2 v = ml(sp);
+        const float w = v.x == -INFINITY ? 0.f : tc::ex2(v.x - M) * v.y;
         s_w[rr * S + sp] = w;
         lsum += w;
       }
@@ -1265,35 +1530,35 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
       for (int sp = lane; sp < S; sp += 32) s_w[rr * S + sp] *= inv;
       if (lane == 0 && p.lse != nullptr) {
-        const int rg = mt_ * kRowsPerTile + r0 + rr;
+        const int rg = g_ * kRowsPerTile + r0 + rr;
         const int node = div_small(rg, p.group_m), qh = h_ * p.group + rg - node * p.group;
         p.lse[node * p.hq + qh] = (M + log2f(lsum)) * 0.69314718055994531f;
       }
     }
     __syncthreads();
-    for (int it = tid; it < items; it += kStepThreads) {
-      const int rr = it / DV, d = (it % DV) * 4;
-      const float* w = s_w + rr * S;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    constexpr int PR = D / 8;
 #pragma unroll 1
-      for (int s0 = 0; s0 < S; s0 += SB) {
-        if (it != tid || s0 != 0) load_batch(it, s0, ov);
+    for (int it = tid; it < nr * PR; it += kStepThreads) {
+      const int rr = it / PR, c = it % PR;
+      const float* w = s_w + rr * S;
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+      for (int sp = 0; sp < S; ++sp) {
+        const uint4 v = *reinterpret_cast<const uint4*>(mst + (static_cast<size_t>(sp) * nr + rr) * RB + c * 16);
+        const float wt = w[sp];
+        const __half2* hv = reinterpret_cast<const __half2*>(&v);
 #pragma unroll
-        for (int u = 0; u < SB; ++u) {
-          if (s0 + u < S) {
-            const float wt = w[s0 + u];
-            const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&ov[u].x));
-            const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&ov[u].y));
-            acc.x += wt * f01.x;
-            acc.y += wt * f01.y;
-            acc.z += wt * f23.x;
-            acc.w += wt * f23.y;
-          }
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(hv[e]);
+          acc[2 * e] += wt * f.x;
+          acc[2 * e + 1] += wt * f.y;
         }
       }
-      const int rg = mt_ * kRowsPerTile + r0 + rr;
+      const int rg = g_ * kRowsPerTile + r0 + rr;
       const int node = div_small(rg, p.group_m), qh = h_ * p.group + rg - node * p.group;
-      *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(node) * p.hq + qh) * D + d) = acc;
+      float4* dst = reinterpret_cast<float4*>(p.out + (static_cast<size_t>(node) * p.hq + qh) * D + c * 8);
+      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
   }
 }
@@ -1301,6 +1566,20 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
 // ---------------------------------------------------------------- host side
 
 static size_t a256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Tile groups of a KV head's `rows` (node, query head) rows: 128-row tiles,
+// and remainder rows of at most kMaxBRows folded into the last tile group
+// (transposed MMAs; head dims >= 128) when there is at least one full tile.
+static void tile_groups(int rows, int head_dim, bool fold, int* n_grp, int* b_rows) {
+  const int full = rows / kRowsPerTile, rem = rows % kRowsPerTile;
+  if (fold && rem > 0 && rem <= kMaxBRows && full >= 1 && head_dim >= 128) {
+    *n_grp = full;
+    *b_rows = rem;
+  } else {
+    *n_grp = full + (rem > 0 ? 1 : 0);
+    *b_rows = 0;
+  }
+}
 
 static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, int cap, int vocab,
                       int logits_dtype, bool with_accept, int kv_fmt, StepPlan* pl) {
@@ -1312,127 +1591,131 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
   const int sms = sm_count();
   pl->grid = sms < kMaxStepGrid ? sms : kMaxStepGrid;
   pl->rows = n_nodes * (hq / hkv);
-  pl->n_mt = (pl->rows + kRowsPerTile - 1) / kRowsPerTile;
+  // The remainder rows are folded into the last tile group only when asked:
+  // their transposed MMAs cost the tensor pipe about as much per chunk as a
+  // second 128-row tile, which otherwise runs on a CTA of its own in parallel.
+  tile_groups(pl->rows, head_dim, kFoldRemainder, &pl->n_grp, &pl->b_rows);
+  pl->has_b = pl->b_rows > 0 ? 1 : 0;
+  pl->nb = pl->b_rows > 16 ? 32 : 16;
+  const long groups = static_cast<long>(hkv) * pl->n_grp;
+  if (groups > pl->grid) return false;                  // more (head, group) pairs than SMs
   const long kbound = window > 0 ? (window - 1 < cap ? window - 1 : cap) : cap;
   const long tb = (kbound + kChunk - 1) / kChunk + (n_nodes + kChunk - 1) / kChunk;
-  long s = pl->grid / (hkv * pl->n_mt);
-  if (s > tb) s = tb;
+  // one chunk per split when that leaves a CTA for the walker; otherwise (long
+  // contexts) every split takes several chunks and a few CTAs stay for the
+  // logits
+  long s;
+  if (groups * tb <= pl->grid - (with_accept ? 1 : 0)) {
+    s = tb;
+  } else {
+    const long keep = with_accept ? (kLongSpares < pl->grid - groups ? kLongSpares : pl->grid - groups) : 0;
+    s = (pl->grid - keep) / groups;
+  }
   if (s > kMaxStepSplits) s = kMaxStepSplits;
-  if (s < 1) return false;                      // more (head, tile) pairs than SMs
+  {
+    // the merge stages every split's share of a group's rows in sK + sV:
+    // at most (rows + splits) rows of D fp16
+    long merge_b;
+    switch (head_dim) {
+      case 64: merge_b = StepSmem<64>::kKBytes + kChunk * 64 * 2; break;
+      case 128: merge_b = StepSmem<128>::kKBytes + kChunk * 128 * 2; break;
+      default: merge_b = StepSmem<256>::kKBytes + kChunk * 256 * 2; break;
+    }
+    while (s > 1 && (kMaxGroupRows + s) * (head_dim * 2 + 16) > merge_b) --s;
+  }
+  if (s < 1) return false;
   pl->splits = static_cast<int>(s);
-  pl->units = hkv * pl->n_mt * pl->splits;
-  const int tile_b = kRowsPerTile * head_dim * 2;        // logits staging bytes
+  pl->units = static_cast<int>(groups) * pl->splits;
+  const int tile_b = kRowsPerTile * head_dim * 2;
   // the walker stages every argmax partial in its Q tile
   const int max_parts = tile_b / static_cast<int>(sizeof(ArgPartial));
   const int esz = logits_dtype == DFV_DTYPE_BF16 ? 2 : 4;
   // the walker: a CTA without an attention unit when there is one
   pl->walker = with_accept ? (pl->grid > pl->units ? pl->grid - 1 : 0) : -1;
   for (int i = 0; i < kMaxStepGrid; ++i) pl->lslot[i] = 0u;
-  pl->lchunks = pl->lunits = pl->lchunk_len = pl->lbulk = pl->lstride = 0;
+  pl->lchunks = pl->lunits = pl->lchunk_len = pl->lbulk = pl->lstride = pl->lper = 0;
   if (with_accept) {
-    // Staged slices go first to the CTAs without an attention unit (the
-    // walker aside), then to the units of a last row tile of at most 32 rows,
-    // then to the other units, the splits holding the tree chunk (whose rows
-    // come straight from global memory) last. Each
-    // CTA stages as many slices as fit its staging bytes. The plan takes the
-    // fewest slices per node that the shortest such prefix of CTAs can hold,
-    // so that the long attention units stay off the logits when the others
-    // suffice; the last tier used shares its slices evenly.
+    // Logits slices are staged (bulk copies into smem) on the CTAs without an
+    // attention unit, the walker aside, in rounds through the two halves of
+    // their staging area (a round: the slices one half holds). The slice
+    // count per node is the one whose even share puts the least work
+    // (bytes plus a fixed cost per slice) on each of those CTAs. Otherwise
+    // every CTA scans slices with plain loads.
     const int cap_c = (vocab + 255) / 256;
-    int spare_b, unit_b;
+    int spare_b;
     switch (head_dim) {
-      case 64: spare_b = StepSmem<64>::kSpareStageBytes; unit_b = StepSmem<64>::kUnitStageBytes; break;
-      case 128: spare_b = StepSmem<128>::kSpareStageBytes; unit_b = StepSmem<128>::kUnitStageBytes; break;
-      default: spare_b = StepSmem<256>::kSpareStageBytes; unit_b = StepSmem<256>::kUnitStageBytes; break;
+      case 64: spare_b = StepSmem<64>::kSpareStageBytes; break;
+      case 128: spare_b = StepSmem<128>::kSpareStageBytes; break;
+      default: spare_b = StepSmem<256>::kSpareStageBytes; break;
     }
-    int octa[kMaxStepGrid], otier[kMaxStepGrid], no = 0;
-    int tcount[4] = {0, 0, 0, 0};
-    for (int b = pl->units; b < pl->grid; ++b)
-      if (b != pl->walker) { octa[no] = b; otier[no++] = 0; ++tcount[0]; }
-    const int last_rows = pl->rows - (pl->n_mt - 1) * kRowsPerTile;
-    const bool light_tile = pl->n_mt > 1 && last_rows <= 32;
-    auto tier = [&](int u) {
-      const int split = u % pl->splits, mt = (u / pl->splits) % pl->n_mt;
-      if (pl->splits > 1 && split == pl->splits - 1) return 3;
-      if (light_tile && mt == pl->n_mt - 1) return 1;
-      return 2;
-    };
-    for (int t = 1; t <= 3; ++t)
+    int unit_b;
+    switch (head_dim) {
+      case 64: unit_b = StepSmem<64>::kUnitStageBytes; break;
+      case 128: unit_b = StepSmem<128>::kUnitStageBytes; break;
+      default: unit_b = StepSmem<256>::kUnitStageBytes; break;
+    }
+    // light units: the splits of a last tile group of at most kMaxBRows real
+    // rows (no remainder folded in); they stage one round at entry and scan
+    // it while their K / V chunk is still in flight
+    int spare[kMaxStepGrid], nsp = 0, light[kMaxStepGrid], nlu = 0;
+    const int last_rows = pl->rows - (pl->n_grp - 1) * kRowsPerTile;
+    if (!pl->has_b && pl->n_grp > 1 && last_rows <= kMaxBRows)
       for (int u = 0; u < pl->units; ++u)
-        if (tier(u) == t) { octa[no] = u; otier[no++] = t; ++tcount[t]; }
+        if ((u / pl->splits) % pl->n_grp == pl->n_grp - 1 && u != pl->walker) light[nlu++] = u;
+    for (int b = pl->units; b < pl->grid; ++b)
+      if (b != pl->walker) spare[nsp++] = b;
     const int align_el = 16 / esz;
-    auto per_cta = [](long stage_b, long sb) {
-      const long c = stage_b / sb;
-      return c < kMaxStagedSlices ? c : static_cast<long>(kMaxStagedSlices);
-    };
-    int best_lc = -1, best_t = 4, best_len = 0;
+    int best_lc = -1, best_len = 0, best_per = 0, best_lu = 0;
     long best_load = 0;
-    if (static_cast<long>(vocab) * esz % 16 == 0) {
+    if (nsp + nlu > 0 && static_cast<long>(vocab) * esz % 16 == 0) {
       const int max_lc = cap_c < max_parts / n_nodes ? cap_c : max_parts / n_nodes;
-      // the lowest tier that can hold every slice (for some slice count),
-      // then the slice count that puts the least work (bytes, plus a fixed
-      // cost per slice) on each CTA of that tier (fewer slices on a tie)
-      for (int pass = 0; pass < 2; ++pass) {
-        for (int lc = 1; lc <= max_lc; ++lc) {
-          const int len = (((vocab + lc - 1) / lc) + align_el - 1) / align_el * align_el;
-          const long sb = static_cast<long>(len) * esz;
-          if (sb > unit_b) continue;
-          const long need = static_cast<long>(n_nodes) * lc;
-          long held = 0;
-          for (int t = 0; t < 4; ++t) {
-            const long cap_t = per_cta(t == 0 ? spare_b : unit_b, sb) * tcount[t];
-            if (held + cap_t >= need) {
-              if (pass == 0) {
-                if (t < best_t) best_t = t;
-              } else if (t == best_t) {
-                const long load = (need - held + tcount[t] - 1) / tcount[t] * (sb + kSliceCostBytes);
-                if (best_lc < 0 || load < best_load) {
-                  best_lc = lc;
-                  best_len = len;
-                  best_load = load;
-                }
-              }
-              break;
-            }
-            held += cap_t;
-          }
+      for (int lc = 1; lc <= max_lc; ++lc) {
+        const int len = (((vocab + lc - 1) / lc) + align_el - 1) / align_el * align_el;
+        const long sb = static_cast<long>(len) * esz;
+        long per = (spare_b / 2) / sb;
+        if (per > kMaxStagedSlices / 2) per = kMaxStagedSlices / 2;
+        const long per_u = nlu > 0 ? (unit_b / sb < per ? unit_b / sb : per) : 0;
+        const long need = static_cast<long>(n_nodes) * lc;
+        const long lu = need < nlu * per_u ? need : nlu * per_u;   // slices on light units
+        const long rest = need - lu;
+        if (rest > 0 && (nsp == 0 || per < 1)) continue;
+        if (lu == 0 && per < 1) continue;
+        const long spare_load = nsp > 0 ? (rest + nsp - 1) / nsp * (sb + kSliceCostBytes) : 0;
+        const long lu_load = nlu > 0 ? (lu + nlu - 1) / nlu * (sb + kSliceCostBytes) : 0;
+        const long load = spare_load > lu_load ? spare_load : lu_load;
+        if (best_lc < 0 || load < best_load) {
+          best_lc = lc;
+          best_len = len;
+          best_per = static_cast<int>(per < 1 ? 1 : per);
+          best_lu = static_cast<int>(lu);
+          best_load = load;
         }
       }
     }
     if (best_lc > 0) {
-      const long sb = static_cast<long>(best_len) * esz;
       pl->lchunks = best_lc;
       pl->lunits = n_nodes * best_lc;
       pl->lchunk_len = best_len;
-      pl->lstride = static_cast<int>(sb);
+      pl->lstride = best_len * esz;
+      pl->lper = best_per;
       pl->lbulk = 1;
-      // tiers before the last fill to capacity; the last shares the rest
-      long before = 0;
-      for (int t = 0; t < best_t; ++t) before += per_cta(t == 0 ? spare_b : unit_b, sb) * tcount[t];
-      if (before > pl->lunits) before = pl->lunits;
-      const long rest = pl->lunits - before;
-      const long per_last = per_cta(best_t == 0 ? spare_b : unit_b, sb);
-      int sl = 0, li = 0;
-      for (int i = 0; i < no && sl < pl->lunits; ++i) {
-        const int t = otier[i];
-        if (t > best_t) break;
-        long c;
-        if (t < best_t) {
-          c = per_cta(t == 0 ? spare_b : unit_b, sb);
-        } else {
-          // even share of `rest` over the tcount[t] CTAs of the last tier
-          c = rest / tcount[t] + (li < rest % tcount[t] ? 1 : 0);
-          ++li;
-        }
-        if (c > per_last && t == best_t) c = per_last;
-        if (c > pl->lunits - sl) c = pl->lunits - sl;
+      int sl = 0;
+      for (int i = 0; i < nlu && sl < best_lu; ++i) {
+        const int c = best_lu / nlu + (i < best_lu % nlu ? 1 : 0);
         if (c > 0) {
-          pl->lslot[octa[i]] = static_cast<uint32_t>(sl) | (static_cast<uint32_t>(c) << 16);
-          sl += static_cast<int>(c);
+          pl->lslot[light[i]] = static_cast<uint32_t>(sl) | (static_cast<uint32_t>(c) << 16);
+          sl += c;
         }
       }
-    }
-    if (!pl->lbulk) {
+      const int rest = pl->lunits - sl;
+      for (int i = 0; i < nsp && sl < pl->lunits; ++i) {
+        const int c = rest / nsp + (i < rest % nsp ? 1 : 0);
+        if (c > 0) {
+          pl->lslot[spare[i]] = static_cast<uint32_t>(sl) | (static_cast<uint32_t>(c) << 16);
+          sl += c;
+        }
+      }
+    } else {
       // plain loads: CTA b takes slices b, b + grid, ...
       const int lim = kLogitVecs * kStepThreads * 16 < tile_b ? kLogitVecs * kStepThreads * 16 : tile_b;
       const int per_l = lim / esz;
@@ -1446,26 +1729,26 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
       pl->lchunk_len = (((vocab + lc - 1) / lc) + align_el - 1) / align_el * align_el;
     }
   }
+  int kbytes;
+  switch (head_dim) {
+    case 64: pl->smem = StepSmem<64>::kBytes; kbytes = StepSmem<64>::kKBytes; break;
+    case 128: pl->smem = StepSmem<128>::kBytes; kbytes = StepSmem<128>::kKBytes; break;
+    default: pl->smem = StepSmem<256>::kBytes; kbytes = StepSmem<256>::kKBytes; break;
+  }
   {
     const long qbytes = static_cast<long>(n_nodes) * hkv * 2 * kv_row_bytes(kv_fmt, head_dim);
-    const long room = static_cast<long>(kChunk) * (head_dim > kChunk ? head_dim : kChunk) * 2;  // sK
-    pl->walker_local = with_accept && pl->grid > pl->units && qbytes <= room ? 1 : 0;
-  }
-  switch (head_dim) {
-    case 64: pl->smem = StepSmem<64>::kBytes; break;
-    case 128: pl->smem = StepSmem<128>::kBytes; break;
-    default: pl->smem = StepSmem<256>::kBytes; break;
+    pl->walker_local = with_accept && pl->grid > pl->units && qbytes <= kbytes ? 1 : 0;
   }
   // staged tree rows: sized for the larger (binary16) row, so one workspace
   // serves either cache format
   const int rowb = kv_row_bytes(DFV_KV_F16, head_dim);
   pl->ws_bar = 0;
-  pl->ws_arg = a256(static_cast<size_t>(4 + 2 * hkv * pl->n_mt + pl->units) * sizeof(unsigned int));
+  pl->ws_arg = a256(static_cast<size_t>(4 + 2 * groups + pl->units) * sizeof(unsigned int));
   pl->ws_qrows = pl->ws_arg + a256(static_cast<size_t>(pl->lunits) * sizeof(ArgPartial));
   pl->ws_ml = pl->ws_qrows + a256(with_accept ? static_cast<size_t>(n_nodes) * hkv * 2 * rowb : 0);
-  const size_t nrow = pl->splits > 1 ? static_cast<size_t>(pl->units) * kRowsPerTile : 0;
-  pl->ws_o = pl->ws_ml + a256(nrow * sizeof(float2));
-  pl->ws_total = pl->ws_o + a256(nrow * head_dim * sizeof(__half));
+  const size_t nrow = pl->splits > 1 ? static_cast<size_t>(pl->units) * kMaxGroupRows : 0;
+  pl->ws_o = pl->ws_ml;
+  pl->ws_total = pl->ws_o + a256(nrow * static_cast<size_t>(head_dim * 2 + 16));
   return true;
 }
 
@@ -1581,7 +1864,10 @@ dfv_status step_launch(bool with_accept, int n_nodes, int max_depth, int hq, int
   p.vocab = vocab;
   p.logits_dtype = logits_dtype;
   p.rows = pl.rows;
-  p.n_mt = pl.n_mt;
+  p.n_grp = pl.n_grp;
+  p.has_b = pl.has_b;
+  p.b_rows = pl.b_rows;
+  p.nb = pl.nb;
   p.splits = pl.splits;
   p.units = pl.units;
   p.lunits = pl.lunits;
@@ -1589,6 +1875,7 @@ dfv_status step_launch(bool with_accept, int n_nodes, int max_depth, int hq, int
   p.lchunk_len = pl.lchunk_len;
   p.lbulk = pl.lbulk;
   p.lstride = pl.lstride;
+  p.lper = pl.lper;
   p.do_accept = with_accept ? 1 : 0;
   // binary16 tree rows are exact in the cache format, so the flag only
   // changes anything for Q4_0
@@ -1616,11 +1903,10 @@ dfv_status step_launch(bool with_accept, int n_nodes, int max_depth, int hq, int
   p.out_tokens = out_tokens;
   char* ws = static_cast<char*>(workspace);
   p.bar = reinterpret_cast<unsigned int*>(ws + pl.ws_bar);
-  p.ready = p.bar + 4 + 2 * hkv * pl.n_mt;
+  p.ready = p.bar + 4 + 2 * hkv * pl.n_grp;
   p.arg_part = reinterpret_cast<ArgPartial*>(ws + pl.ws_arg);
   p.qrows = reinterpret_cast<uint8_t*>(ws + pl.ws_qrows);
-  p.part_ml = reinterpret_cast<float2*>(ws + pl.ws_ml);
-  p.part_o = reinterpret_cast<__half*>(ws + pl.ws_o);
+  p.part = reinterpret_cast<uint8_t*>(ws + pl.ws_o);
   p.status = status;
   switch (head_dim) {
     case 64: return step_launch_d<64>(p, pl, fmt, stream);
