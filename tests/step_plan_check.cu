@@ -54,19 +54,7 @@ static void check(int N, int hq, int hkv, int D, int W, int cap, int V, int dt, 
   CHECK(pl.grid == (g_sms < dfv::kMaxStepGrid ? g_sms : dfv::kMaxStepGrid), "%s grid %d", tag,
         pl.grid);
   CHECK(pl.rows == N * (hq / hkv), "%s rows", tag);
-  // tile groups: 128-row tiles; remainder rows <= 32 folded into the last
-  // group only with a full tile before them and head dim >= 128
-  const int full = pl.rows / 128, rem = pl.rows % 128;
-  if (pl.has_b) {
-    CHECK(D >= 128 && full >= 1 && rem > 0 && rem <= dfv::kMaxBRows, "%s remainder rows", tag);
-    CHECK(pl.n_grp == full && pl.b_rows == rem, "%s groups with remainder", tag);
-    CHECK((pl.nb == 16 || pl.nb == 32) && pl.nb >= pl.b_rows, "%s remainder N %d", tag, pl.nb);
-    CHECK(128 + D + pl.nb + (D / 128) * pl.nb <= 512, "%s TMEM columns", tag);
-  } else {
-    CHECK(pl.b_rows == 0 && pl.n_grp == full + (rem > 0 ? 1 : 0), "%s groups", tag);
-  }
-  CHECK(128 * pl.n_grp + pl.b_rows >= pl.rows && 128 * (pl.n_grp - 1) < pl.rows, "%s rows covered",
-        tag);
+  CHECK(pl.n_grp == (pl.rows + 127) / 128, "%s tiles", tag);
   CHECK(pl.splits >= 1 && pl.units == hkv * pl.n_grp * pl.splits && pl.units <= pl.grid,
         "%s units %d splits %d", tag, pl.units, pl.splits);
   CHECK(pl.walker == (pl.grid > pl.units ? pl.grid - 1 : 0), "%s walker %d", tag, pl.walker);
@@ -96,7 +84,7 @@ static void check(int N, int hq, int hkv, int D, int W, int cap, int V, int dt, 
         // 32 real rows leaves free until its dequant
         const int g = (b / pl.splits) % pl.n_grp;
         const int rows_g = pl.rows - g * 128 < 128 ? pl.rows - g * 128 : 128;
-        CHECK(!pl.has_b && g == pl.n_grp - 1 && rows_g <= 32, "%s unit %d (group %d, %d rows) stages slices",
+        CHECK(g == pl.n_grp - 1 && rows_g <= dfv::kLightRows, "%s unit %d (tile %d, %d rows) stages slices",
               tag, b, g, rows_g);
         CHECK(sn <= pl.lper && static_cast<long>(sn) * pl.lstride <= unit_b,
               "%s unit %d stages %d slices of %d bytes in %d", tag, b, sn, pl.lstride, unit_b);
@@ -115,8 +103,7 @@ static void check(int N, int hq, int hkv, int D, int W, int cap, int V, int dt, 
     int worst = 0;
     for (int g = 0; g < pl.n_grp; ++g) {
       const int a_rows = pl.rows - g * 128 < 128 ? pl.rows - g * 128 : 128;
-      const int rows_t = a_rows + (pl.has_b && g == pl.n_grp - 1 ? pl.b_rows : 0);
-      CHECK(rows_t <= dfv::kMaxGroupRows, "%s group rows %d", tag, rows_t);
+      const int rows_t = a_rows;
       for (int sp = 0; sp < pl.splits; ++sp) {
         const int nr = (sp + 1) * rows_t / pl.splits - sp * rows_t / pl.splits;
         if (nr * pl.splits > worst) worst = nr * pl.splits;
@@ -136,16 +123,15 @@ static void check(int N, int hq, int hkv, int D, int W, int cap, int V, int dt, 
         "%s workspace order", tag);
   if (pl.splits > 1) {
     // partial rows: D fp16 values + (max, sum) + padding each
-    CHECK(pl.ws_total - pl.ws_o >= static_cast<size_t>(pl.units) * dfv::kMaxGroupRows * (D * 2 + 16),
+    CHECK(pl.ws_total - pl.ws_o >= static_cast<size_t>(pl.units) * 128 * (D * 2 + 16),
           "%s partial sizes", tag);
     // the merge stages (rows + splits) partial rows at most in sK + sV
     const long merge_b = kbytes + 128L * D * 2;
-    CHECK((dfv::kMaxGroupRows + pl.splits) * static_cast<long>(D * 2 + 16) <= merge_b,
+    CHECK((128 + pl.splits) * static_cast<long>(D * 2 + 16) <= merge_b,
           "%s merge staging", tag);
   }
-  std::printf("%s: grid %d units %d splits %d groups %d rem %d lunits %d lbulk %d walker_local %d\n",
-              tag, pl.grid, pl.units, pl.splits, pl.n_grp, pl.b_rows, pl.lunits, pl.lbulk,
-              pl.walker_local);
+  std::printf("%s: grid %d units %d splits %d tiles %d lunits %d lbulk %d walker_local %d\n", tag,
+              pl.grid, pl.units, pl.splits, pl.n_grp, pl.lunits, pl.lbulk, pl.walker_local);
 }
 
 int main() {

@@ -3,10 +3,10 @@ tests/step_plan_check.cu (the step kernel's translation unit plus a host
 main, device code only to PTX) and runs it over shapes from head dim 64 to
 256, 1 to 65 nodes, vocabularies from 1 to 262144 and both logits types, on
 devices of 100 to 300 SMs (the grid is capped at 256 CTAs).
-Checked there: the tile groups cover every row (remainder rows folded into
-the last group only where the transposed MMAs apply, within the TMEM
-columns), every logits slice is staged by exactly one CTA without another
-role, a round of staged slices fits half of its staging area, bulk-copied slices stay 16-byte
+Checked there: the 128-row tiles cover every row, every logits slice is
+staged by exactly one CTA (a CTA without a unit, or a unit of a tile of at
+most 32 rows, which stages one round in the smem its tile leaves free), a
+round of staged slices fits half of a staging area, bulk-copied slices stay 16-byte
 aligned, the argmax partials fit the walker's Q tile, the split merge's
 staging fits, and the workspace regions are ordered, aligned and large
 enough."""
@@ -39,9 +39,9 @@ def test_step_plan_invariants(tmp_path):
     assert r.returncode == 0 and not fails, "\n".join(fails[:20])
     assert r.stdout.strip().splitlines()[-1] == "ok (0 failures)"
     # the benchmarked workload is planned as measured: 136 attention units
-    # (4 KV heads x 2 tile groups (128 + 10 rows) x 17 key chunks), logits
-    # slices staged in rounds on the other CTAs, tree rows on the walker
+    # (4 KV heads x 2 tiles (128 + 10 rows) x 17 key chunks), logits slices
+    # staged on the CTAs without a unit and the 10-row tiles' units, tree rows
+    # on the walker
     bench = [l for l in r.stdout.splitlines()
              if l.startswith("sms=152 N=23 hq=24 hkv=4 D=256 W=2048 cap=62912 V=151936 dt=1 fmt=2:")]
-    assert bench and "units 136 splits 17 groups 2 rem 0 " in bench[0] and \
-        "lbulk 1 walker_local 1" in bench[0], bench
+    assert bench and "units 136 splits 17 tiles 2 lunits 92 lbulk 1 walker_local 1" in bench[0], bench

@@ -9,33 +9,31 @@
 // greedy walk, and the commit of the accepted rows in the cache format.
 //
 // One CTA per SM, one launch per step, no grid-wide barrier. CTA roles:
-//   * attention units = (KV head h, tile group of the head's (node, query
-//     head) rows, range of 128-key chunks). A tile group is a 128-row tile
-//     and, in the last group, up to 32 remainder rows (the budget-22 step
-//     has 138 rows per KV head: 128 + 10), so that every K / V chunk is
-//     loaded and decoded once for all of a head's rows. The tree chunk is
-//     processed first, by the last split of each group;
-//   * CTAs without a unit scan the logits; one of them is the walker.
+//   * attention units = (KV head h, 128-row tile of the head's (node, query
+//     head) rows, range of 128-key chunks); the budget-22 step has 138 rows
+//     per KV head, a full tile and a 10-row one. The tree chunk is processed
+//     first, by the last split of each (head, tile) group;
+//   * CTAs without a unit and the units of a short (<= 32-row) tile scan
+//     the logits; a CTA without a unit is the walker.
 // At t = 0 thread 0 reads ctx and starts 1-D bulk copies (TMA engine) of
-// the unit's first K / V chunk (or of the CTA's logits slices), while the
-// other warps load the bf16 Q rows and the tree rows. Then:
-//   * CTAs without a unit scan their staged logits slices into (max, lowest
-//     index) partials; the walker quantises the tree rows into its smem so
-//     that the commit after the walk is a plain copy;
+// the unit's first K / V chunk, warp 0 those of the tile's bf16 Q rows and
+// then of the CTA's logits slices, while the other warps load the tree rows.
+// Then:
+//   * the CTAs holding logits slices scan them into (max, lowest index)
+//     partials; the walker quantises the tree rows into its smem so that the
+//     commit after the walk is a plain copy;
 //   * per chunk: K and V decoded ((q - 8) * d, one rounding; or binary16 rows
-//     copied as they are) into 128-byte-swizzled smem; by tcgen05.mma into
-//     TMEM: S = Q K^T for the 128-row tile (M = 128 rows, N = 128 keys,
-//     K = D) and, for the remainder rows, the transposed S_B^T = K Q_B^T
-//     (M = 128 keys, N = 16 or 32 rows); the masked (window, ancestors)
-//     online softmax of both; then O += P V (M = 128, N = D, K = 128 keys; V
-//     as an MN-major operand) and O_B^T += V^T P_B^T (M = 128 head dims,
-//     N = 16 or 32 rows; V^T is the same smem tile read as an MN-major A).
-//     A running max only moves (O rescaled in TMEM) when a chunk's max
-//     exceeds it by more than 2^8, so P <= 256 fits fp16;
-//   * each split writes its normalised O rows (fp16), max and sum to the
-//     workspace and marks its ready word; the splits of a group wait for one
-//     another (time-bounded waits) and each merges a share of the group's
-//     rows by log-sum-exp;
+//     copied as they are) into 128-byte-swizzled smem; S = Q K^T by
+//     tcgen05.mma into TMEM (M = 128 rows, N = 128 keys, K = D); four
+//     threads per row read S from TMEM, mask (window, ancestors), exchange
+//     the row max, exp2, write P (fp16); O += P V by tcgen05.mma (M = 128,
+//     N = D, K = 128 keys; V as an MN-major operand). The running max only
+//     moves (O rescaled in TMEM) when a chunk's max exceeds it by more than
+//     2^8, so P <= 256 fits fp16;
+//   * each split writes its normalised O rows (fp16) with their max and sum
+//     to the workspace (one bulk copy) and marks its ready word; the splits
+//     of a group wait for one another (time-bounded waits) and each merges a
+//     share of the group's rows by log-sum-exp;
 //   * the walker waits until every other CTA has read ctx and written its
 //     partials, merges the argmax partials, walks the tree in one warp,
 //     copies the staged accepted rows into the cache at C..C+L-1 and
@@ -55,21 +53,18 @@ namespace dfv {
 constexpr int kStepThreads = 512;   // 16 warps; four per TMEM lane quadrant
 constexpr int kRowsPerTile = 128;   // UMMA M of a row tile
 constexpr int kChunk = 128;         // keys per chunk (UMMA N of S, K of P V)
-constexpr int kMaxBRows = 32;       // remainder rows of a tile group (UMMA N of the transposed pair)
-constexpr int kMaxGroupRows = kRowsPerTile + kMaxBRows;
+constexpr int kLightRows = 32;      // a tile of at most this many real rows stages logits
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxStepSplits = 256;
 constexpr int kMaxStepGrid = 256;   // CTAs of one launch at most
 constexpr int kMaxStagedSlices = 8; // logits slices one CTA stages at most
 constexpr long kSliceCostBytes = 65536;  // per-slice scan overhead (a CTA-wide reduction), in bytes of streaming
 constexpr int kLongSpares = 8;      // CTAs left to the logits when the attention could use every SM
-constexpr bool kFoldRemainder = false;   // fold remainder rows into the last tile group
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kLogitVecs = 16;      // 16-byte logits vectors a thread keeps in flight
 
 struct StepPlan {
-  int rows, n_grp, has_b, b_rows, nb, splits, units, grid, lunits, lchunks, lchunk_len, lbulk,
-      lstride, lper, smem;
+  int rows, n_grp, splits, units, grid, lunits, lchunks, lchunk_len, lbulk, lstride, lper, smem;
   int walker, walker_local;
   uint32_t lslot[kMaxStepGrid];   // per CTA: first logits slice | count << 16
   size_t ws_bar, ws_arg, ws_qrows, ws_ml, ws_o, ws_total;
@@ -78,9 +73,7 @@ struct StepPlan {
 struct StepParams {
   int n_nodes, max_depth, hq, hkv, group, window, capacity, vocab, logits_dtype;
   int rows;          // N * group: (node, query head) rows of one KV head
-  int n_grp;         // tile groups per KV head
-  int has_b;         // the last group also holds remainder rows [128 * n_grp, rows)
-  int b_rows, nb;    // remainder rows, and their UMMA N (16 or 32)
+  int n_grp;         // 128-row tiles per KV head
   int splits, units, lunits, lchunks, lchunk_len, lbulk;
   int lstride;       // bytes between staged slices
   int lper;          // staged slices per half of the staging area (one round)
@@ -113,7 +106,7 @@ struct StepParams {
   unsigned int* ready;      // [units] generation + 1 once the unit's partial is written
   ArgPartial* arg_part;     // [lunits]
   uint8_t* qrows;           // [N][Hkv][2][row bytes]
-  uint8_t* part;            // [units][kMaxGroupRows] rows of kPartRowBytes: O / sum (fp16),
+  uint8_t* part;            // [units][128] rows of kPartRowBytes: O / sum (fp16),
                             // then (running max, log2 units; sum)
   uint32_t* status;
   uint32_t lslot[kMaxStepGrid];   // per CTA: first staged logits slice | count << 16
@@ -130,31 +123,27 @@ template <int D>
 struct StepSmem {
   static constexpr int kRowB = D / 32 * 18;
   static constexpr bool kBulk = (kRowB % 16) == 0;
-  static constexpr bool kHasB = D >= 128;   // remainder rows: O_B^T needs M = 128 head dims
   static constexpr int kTileB = kRowsPerTile * D * 2;        // one [128][D] fp16 tile
-  static constexpr int kQ = 0;                               // Q of the 128-row tile
-  static constexpr int kK = kQ + kTileB;                     // K^, then P (and P_B past it)
-  static constexpr int kPB = kChunk * kChunk * 2;            // P_B's offset in sK
+  static constexpr int kQ = 0;                               // Q of the tile
+  static constexpr int kK = kQ + kTileB;                     // K^, then P
   static constexpr int kKBytes0 = kChunk * D * 2;
-  static constexpr int kKBytes1 = kPB + (kHasB ? kMaxBRows * kChunk * 2 : 0);
+  static constexpr int kKBytes1 = kChunk * kChunk * 2;
   static constexpr int kKBytes = kKBytes0 > kKBytes1 ? kKBytes0 : kKBytes1;
   static constexpr int kV = kK + kKBytes;                    // V^; raw K, raw V land at its end first
   static constexpr int kRawK = kChunk * D * 2 - 2 * kChunk * kRowB;   // raw K's offset in sV
   static constexpr int kRawV = kRawK + kChunk * kRowB;                // raw V's offset in sV
   static constexpr int kQStage = kK;                         // bf16 Q rows land here (sK, then sV)
-  static constexpr int kQB = kV + kChunk * D * 2;            // Q of the remainder rows
-  static constexpr int kQBBytes = kHasB ? kMaxBRows * D * 2 : 0;
-  static constexpr int kBars = kQB + kQBBytes;
-  static constexpr int kSpareStageBytes = kQB;               // logits staging of a CTA without a unit
-  // logits staging of a unit whose tile has at most kMaxBRows real rows:
+  static constexpr int kBars = kV + kChunk * D * 2;
+  static constexpr int kSpareStageBytes = kBars;             // logits staging of a CTA without a unit
+  // logits staging of a unit whose tile has at most kLightRows real rows:
   // past its staged Q rows, up to the raw K / V (free until the dequant)
-  static constexpr int kUnitStage = kK + kMaxBRows * D * 2;
+  static constexpr int kUnitStage = kK + kLightRows * D * 2;
   static constexpr int kUnitStageBytes = kV + kRawK - kUnitStage;
   static constexpr int kBytes = kBars + 64 + 1024;           // + alignment slack
   static_assert(2 * kChunk * kRowB <= kChunk * D * 2, "raw K and V fit in sV");
   static_assert(kRawK % 16 == 0 && kRawV % 16 == 0, "bulk-copy destinations 16-byte aligned");
-  static_assert(kMaxGroupRows * D * 2 <= kKBytes + kRawK, "staged Q rows stay clear of raw K / V");
-  static_assert(kMaxGroupRows * (D * 2 + 16) <= kV, "epilogue staging fits in sQ + sK");
+  static_assert(kRowsPerTile * D * 2 <= kKBytes + kRawK, "staged Q rows stay clear of raw K / V");
+  static_assert(kRowsPerTile * (D * 2 + 16) <= kV, "epilogue staging fits in sQ + sK");
 };
 
 // ---------------------------------------------------------------- small helpers
@@ -574,23 +563,18 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
   uint8_t* sQ = smem + L::kQ;
   uint8_t* sK = smem + L::kK;
   uint8_t* sV = smem + L::kV;
-  uint8_t* sQB = smem + L::kQB;
   uint64_t* bar_kv = reinterpret_cast<uint64_t*>(smem + L::kBars);
   uint64_t* bar_mma = bar_kv + 1;
   uint64_t* bar_lg = bar_kv + 2;     // bar_lg[0..1]: the two halves of the logits staging
   uint64_t* bar_lg2 = bar_kv + 3;
   uint64_t* bar_q = bar_kv + 4;
-  uint64_t* bar_mmab = bar_kv + 5;   // the remainder rows' MMAs
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_kv + 6);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_kv + 5);
 
   __shared__ int s_J[kMaxNodes], s_dep[kMaxNodes];
   __shared__ uint32_t s_anc[kMaxNodes][kMaskWords];
   __shared__ int s_row_node[kRowsPerTile], s_row_lo[kRowsPerTile];
-  __shared__ int s_brow_node[kMaxBRows], s_brow_lo[kMaxBRows];
   __shared__ float s_pmax[4][kRowsPerTile];
-  __shared__ float s_bmax[4][kMaxBRows];
   __shared__ float s_l[4][kRowsPerTile];
-  __shared__ float s_bm[kMaxBRows], s_bl[4][kMaxBRows];
   __shared__ int s_ok;
   __shared__ int s_wpar[kMaxNodes], s_wtok[kMaxNodes];
 
@@ -611,8 +595,6 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     grp = (unit / p.splits) % p.n_grp;
     h = unit / (p.splits * p.n_grp);
   }
-  // the last tile group also holds the remainder rows, by transposed MMAs
-  const bool ub = L::kHasB && unit >= 0 && p.has_b && grp == p.n_grp - 1;
   // the context length, read once by thread 0 (with acquire semantics, so
   // that its report to the walker below cannot overtake it) and shared
   // through smem after the first barrier
@@ -650,11 +632,10 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     bulk_g2s(sV + L::kRawK, p.k_cache + off, bytes, bar_kv);
     bulk_g2s(sV + L::kRawV, p.v_cache + off, bytes, bar_kv);
   };
-  // the tile group's rows [128 grp, 128 grp + rows_g): node n's query heads
-  // of KV head h are contiguous, so one bulk copy per node lands the bf16
-  // rows in order at sK (then on into sV, clear of the raw K / V)
-  const int a_rows_g = unit >= 0 ? min(kRowsPerTile, p.rows - grp * kRowsPerTile) : 0;
-  const int rows_g = a_rows_g + (ub ? p.b_rows : 0);
+  // the tile's rows [128 grp, 128 grp + rows_g): node n's query heads of KV
+  // head h are contiguous, so one bulk copy per node lands the bf16 rows in
+  // order at sK (then on into sV, clear of the raw K / V)
+  const int rows_g = unit >= 0 ? min(kRowsPerTile, p.rows - grp * kRowsPerTile) : 0;
   auto issue_q = [&]() {   // by the 32 lanes of warp 0, node n0 + lane + 32 k each
     const int start = grp * kRowsPerTile, end = start + rows_g;
     for (int n = div_small(start, p.group_m) + lane; n * p.group < end; n += 32) {
@@ -724,7 +705,6 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       mbar_init(bar_mma, 1);
       mbar_init(bar_lg, 1);
       mbar_init(bar_q, 1);
-      mbar_init(bar_mmab, 1);
       mbar_init(bar_lg2, 1);
       fence_mbar_init();
       if (!p.pipelined) ctx_and_first_kv();
@@ -836,25 +816,18 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     derive();
   }
   // ---- Q: once the bf16 rows have landed, warps 1..15 convert them into
-  // the fp16 swizzled tiles (the 128-row tile in sQ, the remainder rows in
-  // sQB); rows past the group's are zero
+  // the fp16 swizzled tile in sQ; rows past the tile's are zero
   if (unit >= 0 && li >= 0) {
     if (!wait_bounded([&]() { return mbar_try_wait(bar_q, 0); }) && li == 0)
       report(p.status, DFV_DEV_TIMEOUT);
     const uint8_t* qs = smem + L::kQStage;
-    constexpr int QA = kRowsPerTile * (D / 8);            // pieces of the 128-row tile
-    const int qall = QA + (ub ? p.nb * (D / 8) : 0);
 #pragma unroll 1
-    for (int it = li; it < qall; it += kLoaders) {
+    for (int it = li; it < kRowsPerTile * (D / 8); it += kLoaders) {
       const int row = it / (D / 8), c = it % (D / 8);
-      const bool real = row < kRowsPerTile ? row < a_rows_g : row - kRowsPerTile < p.b_rows;
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (real) {
-        const int srow = row < kRowsPerTile ? row : a_rows_g + (row - kRowsPerTile);
-        v = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(qs + static_cast<size_t>(srow) * D * 2 + c * 16));
-      }
-      if (row < kRowsPerTile) *reinterpret_cast<uint4*>(sQ + tc::sw128_offset(row, c, kRowsPerTile)) = v;
-      else *reinterpret_cast<uint4*>(sQB + tc::sw128_offset(row - kRowsPerTile, c, p.nb)) = v;
+      if (row < rows_g)
+        v = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(qs + static_cast<size_t>(row) * D * 2 + c * 16));
+      *reinterpret_cast<uint4*>(sQ + tc::sw128_offset(row, c, kRowsPerTile)) = v;
     }
   }
   __syncthreads();   // Q converted, tree bookkeeping done
@@ -913,38 +886,21 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         s_row_node[tid] = -1;
         s_row_lo[tid] = 0x7fffffff;
       }
-    } else if (tid < kRowsPerTile + kMaxBRows) {
-      const int rb = tid - kRowsPerTile;
-      if (ub && rb < p.b_rows) {
-        const int node = div_small(p.n_grp * kRowsPerTile + rb, p.group_m);
-        s_brow_node[rb] = node;
-        s_brow_lo[rb] = p.window > 0 ? C + s_dep[node] - p.window + 1 : 0;
-      } else {
-        s_brow_node[rb] = -1;
-        s_brow_lo[rb] = 0x7fffffff;
-      }
     }
     tc::fence_after_sync();
 
     const uint32_t tmem = *s_tmem;
     const uint32_t t_s = tmem;                    // S: columns [0, 128)
     const uint32_t t_o = tmem + kChunk;           // O: columns [128, 128 + D)
-    const uint32_t t_sb = tmem + kChunk + D;      // S_B^T: nb columns (rows), lanes = keys
-    const uint32_t t_ob = t_sb + (ub ? p.nb : 0); // O_B^T: D / 128 blocks of nb columns, lanes = dims
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int r = (warp & 3) * 32 + lane;   // this thread's row (and key of S_B^T, dim of O_B^T)
-    const int hc = warp >> 2;               // its quarter of the keys / of O's columns / of B's rows
-    const int bcols = ub ? p.nb / 4 : 0;    // remainder rows this thread handles: [hc * bcols, +bcols)
+    const int r = (warp & 3) * 32 + lane;   // this thread's row
+    const int hc = warp >> 2;               // its quarter of the keys / of O's columns
     // A warp whose 32 rows all lie past the last row (a padded tile) skips
     // the second half of the softmax and the epilogue: its P rows keep the
     // finite operand values under them, and its O rows reach no output.
     const bool live = grp * kRowsPerTile + (warp & 3) * 32 < p.rows;
-    uint32_t ph_kv = 0, ph_mma = 0, ph_b = 0;
-    bool pend_b = false;   // the remainder rows' last O_B^T MMAs not waited for yet
+    uint32_t ph_kv = 0, ph_mma = 0;
     float m_run = -INFINITY, l_half = 0.f;
-    float mb[8], lb[8];   // remainder rows: running max, this key's share of the sums
-#pragma unroll
-    for (int c = 0; c < 8; ++c) { mb[c] = -INFINITY; lb[c] = 0.f; }
     bool o_valid = false, alive = true;
     const float sc = p.scale_log2;
 
@@ -1095,13 +1051,11 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       fence_proxy_async_smem();
       __syncthreads();
 
-      // ---- S = Q K^T (M = 128 rows, N = 128 keys, K = D), committed on its
-      // own; then, for the remainder rows, S_B^T = K Q_B^T (M = 128 keys,
-      // N = nb rows, K = D), which runs under the tile's softmax
+      // ---- S = Q K^T (M = 128 rows, N = 128 keys, K = D)
       if (tid == 0) {
         tc::fence_after_sync();
         const uint32_t ida = tc::idesc_f16(kRowsPerTile, kChunk);
-        const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK), qb = smem_u32(sQB);
+        const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK);
 #pragma unroll 1
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = static_cast<uint32_t>((kk >> 2) * kRowsPerTile * 128 + (kk & 3) * 32);
@@ -1109,17 +1063,6 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
                       kk > 0 ? 1u : 0u);
         }
         tc::commit(bar_mma);
-        if (ub) {
-          const uint32_t idb = tc::idesc_f16(kChunk, p.nb);
-#pragma unroll 1
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = static_cast<uint32_t>((kk >> 2) * kChunk * 128 + (kk & 3) * 32);
-            const uint32_t offb = static_cast<uint32_t>((kk >> 2) * p.nb * 128 + (kk & 3) * 32);
-            tc::mma_f16(t_sb, tc::smem_desc_sw128(ka + off, 1024), tc::smem_desc_sw128(qb + offb, 1024),
-                        idb, kk > 0 ? 1u : 0u);
-          }
-          tc::commit(bar_mmab);
-        }
       }
       if (!cta_wait(bar_mma, ph_mma, &s_ok, p.status)) { alive = false; break; }
       ph_mma ^= 1u;
@@ -1155,14 +1098,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
           }
         }
         s_pmax[hc][r] = fmaxf(fmaxf(cm[0], cm[1]), fmaxf(cm[2], cm[3]));
-        if (ub) {
-          // S_B^T reads K^ in sK, which P overwrites below: its commit ends
-          // the barrier of the maxima
-          if (!cta_wait(bar_mmab, ph_b, &s_ok, p.status)) { alive = false; break; }
-          ph_b ^= 1u;
-        } else {
-          __syncthreads();
-        }
+        __syncthreads();
         if (live) {
           const float cmax = fmaxf(fmaxf(s_pmax[0][r], s_pmax[1][r]), fmaxf(s_pmax[2][r], s_pmax[3][r]));
           float alpha = 1.f;
@@ -1208,8 +1144,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       tc::fence_before_sync();
       __syncthreads();
 
-      // ---- O += P V (M = 128 rows, N = D, K = 128 keys; V MN-major); it runs
-      // under the remainder rows' softmax
+      // ---- O += P V (M = 128 rows, N = D, K = 128 keys; V MN-major)
       if (tid == 0) {
         tc::fence_after_sync();
         const uint32_t ida = tc::idesc_f16(kRowsPerTile, D, true);
@@ -1225,103 +1160,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         tc::commit(bar_mma);
       }
 
-      // ---- the remainder rows (S_B^T: lanes = keys): one thread per key and
-      // bcols rows, their running max and this key's share of their sums in
-      // registers (every thread of a row computes the same max from the same
-      // partial maxima); then O_B^T += V^T P_B^T (M = 128 dims per block,
-      // N = nb, K = 128 keys; V^T is sV read as an MN-major A operand)
-      if constexpr (L::kHasB) {
-        if (ub) {
-          tc::fence_after_sync();
-          float sb[8];
-          if (bcols == 8) tc::ld8(t_sb + lane_base + hc * 8, sb);
-          else tc::ld4(t_sb + lane_base + hc * 4, sb);
-          const int key = r;   // lane r of S_B^T is key r of the chunk
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            if (c < bcols) {
-              const int rb = hc * bcols + c;
-              const int bn = s_brow_node[rb];
-              bool vis;
-              if (committed) vis = bn >= 0 && key < nk && j0 + key >= s_brow_lo[rb];
-              else vis = bn >= 0 && key < kMaskWords * 32 && ((s_anc[bn][key >> 5] >> (key & 31)) & 1u);
-              const float x = vis ? sb[c] * sc : -INFINITY;
-              sb[c] = x;
-              float mx = x;
-#pragma unroll
-              for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-              if (lane == 0) s_bmax[warp & 3][rb] = mx;
-            }
-          }
-          __syncthreads();
-          float ab[8];
-          bool bres = false;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            ab[c] = 1.f;
-            if (c < bcols) {
-              const int rb = hc * bcols + c;
-              const float cmax = fmaxf(fmaxf(s_bmax[0][rb], s_bmax[1][rb]), fmaxf(s_bmax[2][rb], s_bmax[3][rb]));
-              if (mb[c] == -INFINITY) {
-                mb[c] = cmax;
-              } else if (cmax > mb[c] + kRescaleLog2) {
-                ab[c] = tc::ex2(mb[c] - cmax);
-                bres = true;
-                mb[c] = cmax;
-              }
-              const float pv = tc::ex2(sb[c] - (mb[c] == -INFINITY ? 0.f : mb[c]));
-              lb[c] = lb[c] * ab[c] + pv;
-              // P_B: K-major [nb rows][128 keys] past P in sK
-              *reinterpret_cast<__half*>(sK + L::kPB + tc::sw128_offset(rb, r >> 3, p.nb) + (r & 7) * 2) =
-                  __float2half_rn(pv);
-            }
-          }
-          if (o_valid && __any_sync(0xffffffffu, bres)) {
-            // O_B^T lanes are head dims: this thread's dim r of every 128-dim
-            // block, columns = its remainder rows
-#pragma unroll 1
-            for (int m2 = 0; m2 < D / 128; ++m2) {
-              const uint32_t col = static_cast<uint32_t>(m2 * p.nb + hc * bcols);
-              float ov[8];
-              if (bcols == 8) tc::ld8(t_ob + lane_base + col, ov);
-              else tc::ld4(t_ob + lane_base + col, ov);
-#pragma unroll
-              for (int c = 0; c < 8; ++c) ov[c] *= ab[c];
-              if (bcols == 8) tc::st8(t_ob + lane_base + col, ov);
-              else tc::st4(t_ob + lane_base + col, ov);
-            }
-          }
-          fence_proxy_async_smem();
-          tc::fence_before_sync();
-          __syncthreads();
-          if (tid == 0) {
-            tc::fence_after_sync();
-            const uint32_t idb = tc::idesc_f16(kRowsPerTile, p.nb, false, true);
-            const uint32_t va = smem_u32(sV), pb = smem_u32(sK) + L::kPB;
-#pragma unroll 1
-            for (int kk = 0; kk < kChunk / 16; ++kk) {
-              const uint32_t offv = static_cast<uint32_t>(kk * 16 * 128);
-              const uint32_t offb = static_cast<uint32_t>((kk >> 2) * p.nb * 128 + (kk & 3) * 32);
-#pragma unroll
-              for (int m2 = 0; m2 < D / 128; ++m2)
-                tc::mma_f16(t_ob + m2 * p.nb,
-                            tc::smem_desc_sw128_mn(va + m2 * 2 * kChunk * 128 + offv, kChunk * 128, 1024),
-                            tc::smem_desc_sw128(pb + offb, 1024), idb, (o_valid || kk > 0) ? 1u : 0u);
-            }
-            tc::commit(bar_mmab);
-          }
-          pend_b = true;
-        }
-      }
       if (!cta_wait(bar_mma, ph_mma, &s_ok, p.status)) { alive = false; break; }
       ph_mma ^= 1u;
-      // the next chunk overwrites sK / sV: the remainder rows' MMAs too must
-      // be done (the last chunk's are waited for after the tile's epilogue)
-      if (pend_b && i + 1 < c1 - c0) {
-        if (!cta_wait(bar_mmab, ph_b, &s_ok, p.status)) { alive = false; break; }
-        ph_b ^= 1u;
-        pend_b = false;
-      }
       o_valid = true;
       tc::fence_after_sync();
     }
@@ -1332,32 +1172,14 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     // copy to the workspace; or straight to the output (fp32) when there is
     // one split
     s_l[hc][r] = l_half;
-    if constexpr (L::kHasB) {
-      if (ub) {
-        // the remainder rows' sums over this warp's 32 keys, then (below)
-        // over the four lane quadrants
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          if (c < bcols) {
-            float v = lb[c];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (lane == 0) {
-              s_bl[warp & 3][hc * bcols + c] = v;
-              if ((warp & 3) == 0) s_bm[hc * bcols + c] = mb[c];
-            }
-          }
-        }
-      }
-    }
     __syncthreads();
-    bool ok_all = o_valid && alive;
+    const bool ok_all = o_valid && alive;
     constexpr int RB = kPartRowBytes<D>;   // bytes of one partial row
     uint8_t* stage = smem;                 // [rows_g][RB], over sQ and sK (free after the last MMA)
     if (ok_all && live) {
       // the TMEM loads are warp-wide (.sync.aligned): every lane loads, the
       // lanes of real rows store
-      const bool mine = r < a_rows_g;
+      const bool mine = r < rows_g;
       const float l = (s_l[0][r] + s_l[1][r]) + (s_l[2][r] + s_l[3][r]);
       const float inv = l > 0.f ? __fdividef(1.f, l) : 0.f;
       constexpr int CT = D / 4;            // columns of this thread
@@ -1388,60 +1210,11 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         }
       }
     }
-    if (pend_b) {
-      // the remainder rows' last O_B^T MMAs, which ran under the tile's
-      // epilogue (waited for even after a timeout: TMEM is freed below)
-      if (!cta_wait(bar_mmab, ph_b, &s_ok, p.status)) ok_all = false;
-      ph_b ^= 1u;
-      pend_b = false;
-      tc::fence_after_sync();
-    }
-    if constexpr (L::kHasB) {
-      if (ub && ok_all) {
-        // O_B^T: lane = dim r of each 128-dim block, columns = remainder
-        // rows; both blocks in one batch of loads
-        float ov[16];
-        const uint32_t col0 = t_ob + lane_base + hc * bcols;
-        if constexpr (D / 128 == 2) {
-          if (bcols == 8) tc::ld8x2(col0, col0 + p.nb, ov);
-          else tc::ld4x2(col0, col0 + p.nb, ov);
-        } else {
-          if (bcols == 8) tc::ld8(col0, ov);
-          else tc::ld4(col0, ov);
-        }
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int rb = hc * bcols + c;
-          if (c < bcols && rb < p.b_rows) {
-            const float l = (s_bl[0][rb] + s_bl[1][rb]) + (s_bl[2][rb] + s_bl[3][rb]);
-            const float inv = l > 0.f ? __fdividef(1.f, l) : 0.f;
-            const int row = kRowsPerTile + rb;
-            const int rg = p.n_grp * kRowsPerTile + rb;
-            const int node = div_small(rg, p.group_m), qh = h * p.group + rg - node * p.group;
-#pragma unroll
-            for (int m2 = 0; m2 < D / 128; ++m2) {
-              const int d = m2 * 128 + r;
-              const float v = (bcols == 8 ? ov[m2 * 8 + c] : ov[(m2 * 4 + c) & 15]) * inv;
-              if (p.splits == 1) p.out[(static_cast<size_t>(node) * p.hq + qh) * D + d] = v;
-              else *reinterpret_cast<__half*>(stage + row * RB + d * 2) = __float2half_rn(v);
-            }
-            if (lane == 0 && (warp & 3) == 0) {
-              if (p.splits == 1) {
-                if (p.lse != nullptr) p.lse[node * p.hq + qh] = (s_bm[rb] + log2f(l)) * 0.69314718055994531f;
-              } else {
-                *reinterpret_cast<float2*>(stage + row * RB + D * 2) =
-                    make_float2(l > 0.f ? s_bm[rb] : -INFINITY, l);
-              }
-            }
-          }
-        }
-      }
-    }
     tc::fence_before_sync();
     fence_proxy_async_smem();   // the staged rows, before the bulk copy reads them
     __syncthreads();
     if (p.splits > 1) {
-      uint8_t* part = p.part + static_cast<size_t>(unit) * kMaxGroupRows * RB;
+      uint8_t* part = p.part + static_cast<size_t>(unit) * kRowsPerTile * RB;
       if (!ok_all) {
         // a timed-out unit publishes empty rows (max -inf, sum 0): the merge
         // leaves it out (the status reports the timeout)
@@ -1492,8 +1265,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     __syncthreads();
     if (!s_ok) return;
     const int h_ = gi / p.n_grp, g_ = gi % p.n_grp;
-    const bool ub_ = p.has_b && g_ == p.n_grp - 1;
-    const int rows_t = min(kRowsPerTile, p.rows - g_ * kRowsPerTile) + (ub_ ? p.b_rows : 0);
+    const int rows_t = min(kRowsPerTile, p.rows - g_ * kRowsPerTile);
     const int r0 = split_ * rows_t / p.splits, r1 = (split_ + 1) * rows_t / p.splits;
     const int nr = r1 - r0, S = p.splits;
     if (nr <= 0) return;
@@ -1503,7 +1275,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       fence_proxy_async_global();   // the acquired partials, before the async-proxy reads
       mbar_arrive_expect_tx(bar_q, static_cast<uint32_t>(S * nr * RB));
       for (int s = 0; s < S; ++s)
-        bulk_g2s(mst + static_cast<size_t>(s) * nr * RB, p.part + ((ubase + s) * kMaxGroupRows + r0) * RB,
+        bulk_g2s(mst + static_cast<size_t>(s) * nr * RB, p.part + ((ubase + s) * kRowsPerTile + r0) * RB,
                  static_cast<uint32_t>(nr * RB), bar_q);
     }
     if (!wait_bounded([&]() { return mbar_try_wait(bar_q, 1); })) {
@@ -1567,20 +1339,6 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
 
 static size_t a256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Tile groups of a KV head's `rows` (node, query head) rows: 128-row tiles,
-// and remainder rows of at most kMaxBRows folded into the last tile group
-// (transposed MMAs; head dims >= 128) when there is at least one full tile.
-static void tile_groups(int rows, int head_dim, bool fold, int* n_grp, int* b_rows) {
-  const int full = rows / kRowsPerTile, rem = rows % kRowsPerTile;
-  if (fold && rem > 0 && rem <= kMaxBRows && full >= 1 && head_dim >= 128) {
-    *n_grp = full;
-    *b_rows = rem;
-  } else {
-    *n_grp = full + (rem > 0 ? 1 : 0);
-    *b_rows = 0;
-  }
-}
-
 static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, int cap, int vocab,
                       int logits_dtype, bool with_accept, int kv_fmt, StepPlan* pl) {
   if (n_nodes < 1 || n_nodes > kMaxNodes || hkv < 1 || hq < hkv || hq % hkv || hq > 256 ||
@@ -1591,12 +1349,7 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
   const int sms = sm_count();
   pl->grid = sms < kMaxStepGrid ? sms : kMaxStepGrid;
   pl->rows = n_nodes * (hq / hkv);
-  // The remainder rows are folded into the last tile group only when asked:
-  // their transposed MMAs cost the tensor pipe about as much per chunk as a
-  // second 128-row tile, which otherwise runs on a CTA of its own in parallel.
-  tile_groups(pl->rows, head_dim, kFoldRemainder, &pl->n_grp, &pl->b_rows);
-  pl->has_b = pl->b_rows > 0 ? 1 : 0;
-  pl->nb = pl->b_rows > 16 ? 32 : 16;
+  pl->n_grp = (pl->rows + kRowsPerTile - 1) / kRowsPerTile;   // 128-row tiles per KV head
   const long groups = static_cast<long>(hkv) * pl->n_grp;
   if (groups > pl->grid) return false;                  // more (head, group) pairs than SMs
   const long kbound = window > 0 ? (window - 1 < cap ? window - 1 : cap) : cap;
@@ -1621,7 +1374,7 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
       case 128: merge_b = StepSmem<128>::kKBytes + kChunk * 128 * 2; break;
       default: merge_b = StepSmem<256>::kKBytes + kChunk * 256 * 2; break;
     }
-    while (s > 1 && (kMaxGroupRows + s) * (head_dim * 2 + 16) > merge_b) --s;
+    while (s > 1 && (kRowsPerTile + s) * (head_dim * 2 + 16) > merge_b) --s;
   }
   if (s < 1) return false;
   pl->splits = static_cast<int>(s);
@@ -1654,12 +1407,12 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
       case 128: unit_b = StepSmem<128>::kUnitStageBytes; break;
       default: unit_b = StepSmem<256>::kUnitStageBytes; break;
     }
-    // light units: the splits of a last tile group of at most kMaxBRows real
+    // light units: the splits of a last tile of at most kLightRows real
     // rows (no remainder folded in); they stage one round at entry and scan
     // it while their K / V chunk is still in flight
     int spare[kMaxStepGrid], nsp = 0, light[kMaxStepGrid], nlu = 0;
     const int last_rows = pl->rows - (pl->n_grp - 1) * kRowsPerTile;
-    if (!pl->has_b && pl->n_grp > 1 && last_rows <= kMaxBRows)
+    if (pl->n_grp > 1 && last_rows <= kLightRows)
       for (int u = 0; u < pl->units; ++u)
         if ((u / pl->splits) % pl->n_grp == pl->n_grp - 1 && u != pl->walker) light[nlu++] = u;
     for (int b = pl->units; b < pl->grid; ++b)
@@ -1746,7 +1499,7 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
   pl->ws_arg = a256(static_cast<size_t>(4 + 2 * groups + pl->units) * sizeof(unsigned int));
   pl->ws_qrows = pl->ws_arg + a256(static_cast<size_t>(pl->lunits) * sizeof(ArgPartial));
   pl->ws_ml = pl->ws_qrows + a256(with_accept ? static_cast<size_t>(n_nodes) * hkv * 2 * rowb : 0);
-  const size_t nrow = pl->splits > 1 ? static_cast<size_t>(pl->units) * kMaxGroupRows : 0;
+  const size_t nrow = pl->splits > 1 ? static_cast<size_t>(pl->units) * kRowsPerTile : 0;
   pl->ws_o = pl->ws_ml;
   pl->ws_total = pl->ws_o + a256(nrow * static_cast<size_t>(head_dim * 2 + 16));
   return true;
@@ -1865,9 +1618,6 @@ dfv_status step_launch(bool with_accept, int n_nodes, int max_depth, int hq, int
   p.logits_dtype = logits_dtype;
   p.rows = pl.rows;
   p.n_grp = pl.n_grp;
-  p.has_b = pl.has_b;
-  p.b_rows = pl.b_rows;
-  p.nb = pl.nb;
   p.splits = pl.splits;
   p.units = pl.units;
   p.lunits = pl.lunits;
