@@ -85,6 +85,11 @@ typedef enum dfv_status {
                                /* committed; attention uses it clamped       */
 #define DFV_DEV_BAD_PATH 0x10u /* path entry outside [0, n_nodes): no write   */
 #define DFV_DEV_TIMEOUT 0x20u  /* a bounded wait gave up; outputs undefined   */
+/* Every wait of a kernel (on a copy, an MMA, or another CTA of the step)
+ * gives up after 100 ms of the GPU's global timer and sets DFV_DEV_TIMEOUT;
+ * the kernel then skips what depended on the wait (a walker that timed out
+ * commits nothing) and returns. Clear the workspace (dfv_workspace_clear)
+ * before using it again after a timeout. */
 
 #define DFV_KV_F16 1  /* binary16 values, 2 * D bytes per row                */
 #define DFV_KV_Q4_0 2 /* Q4_0 blocks, D / 32 * 18 bytes per row               */

@@ -164,6 +164,14 @@ def workspace(nbytes, device="cuda", stream=None):
     return ws
 
 
+def clear_workspace(ws, stream=None):
+    """Zero a workspace on the device (dfv_workspace_clear): before its first
+    use, and again after a step reported DFV_DEV_TIMEOUT."""
+    _dev(ws, "workspace", (torch.uint8,))
+    _check(lib().dfv_workspace_clear(ws.data_ptr(), ws.numel(), _stream(stream)),
+           "dfv_workspace_clear")
+
+
 def tree_verify_attn(cache, q, tree_k, tree_v, parent, window, max_depth, out, lse, ws,
                      scale=0.0, status=None, stream=None, tree_as_cache=False, pipelined=False):
     n, hq, d = q.shape
