@@ -11,7 +11,13 @@ Inputs larger than L2: 64 distinct step inputs (7.4 MB each) and 64 KV-cache
 replicas (one per step modulo 64, standing in for a model's attention
 layers) are cycled, so every step reads its KV window and logits from HBM.
 
+--workload full times the whole 131072-token context without a window
+(tensor-bound; reported against the bf16 tensor roof with the HBM fraction
+beside it), --workload short the 4096-token context; --oracle-replay S
+times only the oracle over S chained steps of the 61440-token workload.
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                       [--workload long|full|short]
 Prints one JSON line (rank 0).
 """
 
@@ -33,6 +39,20 @@ UNIT = "steps/s"
 WORKLOAD = "long_ctx61440_w2048_b22"
 POOL = 64        # distinct step inputs
 REPLICAS = 64    # KV-cache replicas
+# --workload: the headline 61440-token step (default), the full 131072-token
+# context without a window, and the 4096-token short context
+METRICS = {"long": METRIC,
+           "full": "verify steps/s @ctx 131072 (no window), budget 22; attention TFLOP/s and "
+                   "% of GB300 bf16 peak",
+           "short": "verify steps/s @ctx 4096, window 2048, budget 22"}
+WORKLOADS = {"long": ("LONG_WINDOW", "long_ctx61440_w2048_b22"),
+             "full": ("FULL_LONG", "full_ctx131072_nowindow_b22"),
+             "short": ("SHORT", "short_ctx4096_w2048_b22")}
+
+
+def workload_cfg(name):
+    from tree_verify_attention_gb300 import workload as W
+    return getattr(W, WORKLOADS[name][0]), WORKLOADS[name][1]
 
 
 def parse_args(argv=None):
@@ -46,7 +66,15 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pool", type=int, default=POOL, help="distinct step inputs")
-    ap.add_argument("--replicas", type=int, default=REPLICAS, help="KV-cache replicas")
+    ap.add_argument("--replicas", type=int, default=None,
+                    help="KV-cache replicas (default 64; 4 for the full context, whose "
+                         "cache alone is larger than L2)")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="long",
+                    help="long: ctx 61440, window 2048 (the headline); full: ctx 131072, no "
+                         "window (tensor-bound); short: ctx 4096, window 2048")
+    ap.add_argument("--oracle-replay", type=int, default=0, metavar="STEPS",
+                    help="only time the oracle replaying STEPS chained steps of the long "
+                         "workload (one thread) and print one JSON line")
     ap.add_argument("--cpu-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--cpu-start-at", type=float, default=0.0, help=argparse.SUPPRESS)
     ap.add_argument("--clock-log", default=None,
@@ -149,15 +177,19 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- CPU oracle timing
 
-def cpu_oracle_child(seconds, max_steps, start_at=0.0, warmup=0):
+def cpu_oracle_child(seconds, max_steps, start_at=0.0, warmup=0, workload="long"):
     """Time the oracle's whole verify step on a bounded sample of the
     workload (runs in a single-threaded child process). With ``start_at``
     (a wall-clock time) the timed loop starts then and runs for ``seconds``,
-    so that concurrent children overlap."""
+    so that concurrent children overlap. The full 131072-token context takes
+    minutes per oracle step: there a sample of (node, query head) rows is
+    timed and scaled to a step (see cpu_oracle_sampled)."""
     import numpy as np
     import oracle
     from tree_verify_attention_gb300 import workload as W
-    cfg = W.LONG_WINDOW
+    cfg, _ = workload_cfg(workload)
+    if cfg.window == 0 and cfg.ctx_len > 65536:
+        return cpu_oracle_sampled(cfg, seconds)
     kf, vf = W.make_context(cfg)
     cap = cfg.ctx_len + 64 * cfg.n_nodes
     kc = np.zeros((cfg.n_kv_heads, cap, cfg.head_dim // 32, 18), np.uint8)
@@ -191,7 +223,94 @@ def cpu_oracle_child(seconds, max_steps, start_at=0.0, warmup=0):
                       "late": int(start_at > 0 and time.time() - el > start_at + 1.0)}))
 
 
-def run_cpu_oracle_all_cores(seconds, max_procs=32):
+def cpu_oracle_sampled(cfg, seconds):
+    """Oracle time of one step at a context too long to run whole: the
+    oracle's cache dequantisation (every committed row of every KV head),
+    its per-node argmax, walk and commit are timed once each, its attention
+    on (node, query head) rows one at a time (oracle.attention.attention_one,
+    the same concatenate-and-softmax per row as the full oracle) for about
+    ``seconds``; the step time is the fixed parts plus the per-row time x all
+    rows."""
+    import numpy as np
+    import oracle
+    from tree_verify_attention_gb300 import workload as W
+    kf, vf = W.make_context(cfg)
+    cap = cfg.ctx_len + 2 * cfg.n_nodes
+    kc = np.zeros((cfg.n_kv_heads, cap, cfg.head_dim // 32, 18), np.uint8)
+    vc = np.zeros_like(kc)
+    kc[:, :cfg.ctx_len] = oracle.q4_0.quantize_rows(kf)
+    vc[:, :cfg.ctx_len] = oracle.q4_0.quantize_rows(vf)
+    del kf, vf
+    s = W.make_step(cfg, 0)
+    C = cfg.ctx_len
+    t0 = time.perf_counter()
+    kd = oracle.q4_0.dequantize_rows(kc[:, :C])
+    vd = oracle.q4_0.dequantize_rows(vc[:, :C])
+    t_deq = time.perf_counter() - t0
+    q, kt, vt = (W.bf16_bits_to_f32(s.q), W.bf16_bits_to_f32(s.k_tree), W.bf16_bits_to_f32(s.v_tree))
+    g = cfg.n_q_heads // cfg.n_kv_heads
+    rows, t0 = 0, time.perf_counter()
+    while True:
+        node, h = rows % cfg.n_nodes, (rows * 7) % cfg.n_q_heads
+        oracle.attention.attention_one(q[node, h], kd[h // g], vd[h // g], kt[:, h // g], vt[:, h // g],
+                                       s.parent, C, cfg.window, node)
+        rows += 1
+        el = time.perf_counter() - t0
+        if el >= seconds and rows >= 2:
+            break
+    t_row = el / rows
+    t0 = time.perf_counter()
+    am = oracle.accept.node_argmax(W.bf16_bits_to_f32(s.logits))
+    path, _ = oracle.accept.greedy_walk(s.parent, s.tokens, am)
+    oracle.commit.kv_commit(kc, vc, C, path, kt, vt)
+    t_acc = time.perf_counter() - t0
+    n_rows = cfg.n_nodes * cfg.n_q_heads
+    t_step = t_deq + t_row * n_rows + t_acc
+    print(json.dumps({"steps": 1, "seconds": t_step, "value": 1.0 / t_step, "warmup": 0, "late": 0,
+                      "sampled": {"rows_timed": rows, "rows_per_step": n_rows, "row_s": t_row,
+                                  "dequant_s": t_deq, "accept_commit_s": t_acc}}))
+
+
+def oracle_replay(steps):
+    """Time the oracle replaying ``steps`` chained verify steps of the long
+    workload from a fresh cache (the sequence the chained parity test
+    checks: step i's inputs are make_step(cfg, i), each step starts at the
+    previous step's committed length). Generating the inputs is not timed.
+    NumPy may use every host thread; the count is reported."""
+    import numpy as np
+    import oracle
+    from tree_verify_attention_gb300 import workload as W
+    cfg = W.LONG_WINDOW
+    kf, vf = W.make_context(cfg)
+    cap = cfg.ctx_len + steps * cfg.n_nodes
+    kc = np.zeros((cfg.n_kv_heads, cap, cfg.head_dim // 32, 18), np.uint8)
+    vc = np.zeros_like(kc)
+    kc[:, :cfg.ctx_len] = oracle.q4_0.quantize_rows(kf)
+    vc[:, :cfg.ctx_len] = oracle.q4_0.quantize_rows(vf)
+    del kf, vf
+    ctx, total, accepted = cfg.ctx_len, 0.0, 0
+    for i in range(steps):
+        s = W.make_step(cfg, i)
+        args = (W.bf16_bits_to_f32(s.q), W.bf16_bits_to_f32(s.k_tree),
+                W.bf16_bits_to_f32(s.v_tree), s.parent, s.tokens, W.bf16_bits_to_f32(s.logits))
+        t0 = time.perf_counter()
+        r = oracle.step.verify_step(kc, vc, ctx, cfg.window, *args)
+        total += time.perf_counter() - t0
+        accepted += r["ctx_len"] - ctx
+        ctx = r["ctx_len"]
+    threads = None
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max((d.get("num_threads", 1) for d in threadpool_info()), default=1)
+    except Exception:
+        threads = os.environ.get("OMP_NUM_THREADS")
+    print(json.dumps({"oracle_replay": cfg.name, "steps": steps, "seconds": total,
+                      "s_per_step": total / steps, "final_ctx": ctx, "accepted_rows": accepted,
+                      "host_cores": len(os.sched_getaffinity(0)), "blas_threads": threads}),
+          flush=True)
+
+
+def run_cpu_oracle_all_cores(seconds, workload="long", max_procs=32):
     """The same oracle on every host core at once: one single-threaded child
     per core, each on its own sequence, timed loops aligned to one start
     time; the value is the sum of the children's steps/s."""
@@ -202,7 +321,8 @@ def run_cpu_oracle_all_cores(seconds, max_procs=32):
     env["CUDA_VISIBLE_DEVICES"] = ""
     start_at = time.time() + 30.0            # after every child's setup
     procs = [subprocess.Popen([sys.executable, os.path.abspath(__file__), "--cpu-child",
-                               "--cpu-seconds", str(seconds), "--cpu-start-at", str(start_at)],
+                               "--cpu-seconds", str(seconds), "--cpu-start-at", str(start_at),
+                               "--workload", workload],
                               env=env, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
              for _ in range(cores)]
     rates, steps, late = [], 0, 0
@@ -216,26 +336,36 @@ def run_cpu_oracle_all_cores(seconds, max_procs=32):
         late += int(res.get("late", 0))
     return {"value": sum(rates), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": (f"{cores} single-threaded oracle processes, one sequence each "
-                       f"(verify_step at ctx 61440), timed loops of {seconds:.0f} s started "
+                       f"(verify_step, workload {workload}), timed loops of {seconds:.0f} s started "
                        f"together ({late} started late): {steps} steps in all")}
 
 
-def run_cpu_oracle(seconds, max_steps=10 ** 9, warmup=0):
+def run_cpu_oracle(seconds, max_steps=10 ** 9, warmup=0, workload="long"):
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = "1"
     env["CUDA_VISIBLE_DEVICES"] = ""
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-child",
                         "--cpu-seconds", str(seconds), "--steps", str(max_steps),
-                        "--warmup", str(warmup)],
+                        "--warmup", str(warmup), "--workload", workload],
                        env=env, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("CPU oracle timing failed:\n" + r.stderr[-2000:])
     res = json.loads(r.stdout.strip().splitlines()[-1])
-    res["sample"] = (f"oracle verify_step (fp64 tree attention over the 2047-key window, "
-                     f"23 x 151936 argmax, greedy walk, Q4_0 commit) at ctx 61440: "
-                     f"{res['steps']} consecutive steps after {res['warmup']} untimed ones, "
-                     f"{res['seconds']:.1f} s, one thread")
+    cfg, _ = workload_cfg(workload)
+    keys = f"the {cfg.window - 1}-key window" if cfg.window else f"all {cfg.ctx_len} keys"
+    if "sampled" in res:
+        sp = res["sampled"]
+        res["sample"] = (f"oracle at ctx {cfg.ctx_len} (no window), one thread: cache dequantisation "
+                         f"{sp['dequant_s']:.1f} s, argmax + walk + commit {sp['accept_commit_s']:.2f} s, "
+                         f"fp64 attention timed on {sp['rows_timed']} (node, head) rows at "
+                         f"{sp['row_s'] * 1e3:.0f} ms each and scaled to the step's "
+                         f"{sp['rows_per_step']} rows: {res['seconds']:.1f} s per step")
+    else:
+        res["sample"] = (f"oracle verify_step (fp64 tree attention over {keys}, "
+                         f"{cfg.n_nodes} x {cfg.vocab} argmax, greedy walk, Q4_0 commit) at ctx "
+                         f"{cfg.ctx_len}: {res['steps']} consecutive steps after {res['warmup']} "
+                         f"untimed ones, {res['seconds']:.1f} s, one thread")
     return res
 
 
@@ -245,16 +375,21 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
+    cfg, wname = workload_cfg(args.workload)
+    full = args.workload == "full"
     res = run_cpu_oracle(seconds=min(60.0, args.cpu_seconds * 4), max_steps=args.steps,
-                         warmup=min(10, max(3, args.warmup)))
+                         warmup=0 if full else min(10, max(3, args.warmup)),
+                         workload=args.workload)
     cpu = {"value": res["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
            "sample": res["sample"]}
-    line = {"impl": "reference", "metric": METRIC, "value": res["value"], "unit": UNIT,
+    line = {"impl": "reference", "metric": METRICS[args.workload], "value": res["value"], "unit": UNIT,
             "n_gpus": args.gpus, "steps": res["steps"], "warmup": res["warmup"],
             "ms_per_step": 1000.0 * res["seconds"] / res["steps"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "ctx": 61440, "window": 2048, "budget": 22,
-                       "heads": "24/4", "head_dim": 256, "vocab": 151936},
+            "config": {"workload": wname, "ctx": cfg.ctx_len, "window": cfg.window,
+                       "budget": cfg.n_nodes - 1,
+                       "heads": f"{cfg.n_q_heads}/{cfg.n_kv_heads}", "head_dim": cfg.head_dim,
+                       "vocab": cfg.vocab},
             "cpu_baseline": cpu,
             "e2e": {"value": res["value"], "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -381,12 +516,14 @@ def run_gpu(args):
     from tree_verify_attention_gb300 import api, build
     from tree_verify_attention_gb300 import workload as W
     build.build()
-    cfg = W.LONG_WINDOW
+    cfg, wname = workload_cfg(args.workload)
+    full = args.workload == "full"
     N, hq, hkv, D, Wn, V, C = (cfg.n_nodes, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim,
                                cfg.window, cfg.vocab, cfg.ctx_len)
     K, Wu = args.steps, max(3, args.warmup)
     per_phase = max(K, Wu, args.e2e_steps, args.probe_steps)
-    n_pool, n_rep = args.pool, args.replicas
+    n_pool = args.pool
+    n_rep = args.replicas or (4 if full else REPLICAS)
     cap = C + (math.ceil(per_phase / n_rep) + 2) * N
     row = api.row_bytes(D, args.fmt)
 
@@ -527,7 +664,7 @@ def run_gpu(args):
     kvlg_gbs = (kv_b + lg_b) * per_rank_sps / 1e9
     peaks = _peaks()
     hbm = peaks.get("hbm_gbs") or 6800.0
-    tf = peaks.get("bf16_tflops") or 1900.0
+    tf = peaks.get("bf16_tflops_sustained") or 1700.0
     peak_src = "measured" if peaks else "fallback"
 
     # the step kernel's average launch duration: CUDA events around the timed
@@ -540,43 +677,49 @@ def run_gpu(args):
             "kv_logits_gbs": (kv_b + lg_b) / t_launch / 1e9,
             "attention_tflops": flops / t_launch / 1e12},
     }
-    roof = {"kernel": "step_kernel<256>", "bound": "hbm",
-            "achieved": (kv_b + lg_b) / t_launch / 1e9, "peak": hbm, "unit": "GB/s",
-            "frac": (kv_b + lg_b) / t_launch / 1e9 / hbm,
-            "traffic": recorded_traffic(args.fmt, args.tree_as_cache),
-            "peak_source": peak_src + " copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
-            "duration": "CUDA events over the timed graph region / launches",
-            "algorithmic_bytes": kv_b + lg_b,
-            "tensor_tflops": flops / t_launch / 1e12, "tensor_peak": tf}
+    gbs, tfs = (kv_b + lg_b) / t_launch / 1e9, flops / t_launch / 1e12
+    hbm_roof = {"achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                "peak_source": peak_src + " copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                "algorithmic_bytes": kv_b + lg_b}
+    tensor_roof = {"achieved": tfs, "peak": tf, "unit": "TFLOP/s", "frac": tfs / tf,
+                   "peak_source": peak_src + " sustained bf16 GEMM (MEASURED_PEAKS.json "
+                                  "bf16_tflops_sustained; fp16 runs at the bf16 rate)",
+                   "algorithmic_flops": flops}
+    # the full context does 469 flop per byte, above the ridge (~255): tensor-bound
+    roof = dict(tensor_roof if full else hbm_roof)
+    roof.update({"kernel": "step_kernel<256>", "bound": "tensor" if full else "hbm",
+                 "traffic": recorded_traffic(args.fmt, args.tree_as_cache, wname),
+                 "duration": "CUDA events over the timed graph region / launches",
+                 "hbm": hbm_roof, "tensor": tensor_roof})
 
     cpu = cpu_all = None
     if rank == 0 and not args.no_cpu_baseline:
         try:
-            r = run_cpu_oracle(args.cpu_seconds, warmup=3)
+            r = run_cpu_oracle(args.cpu_seconds, warmup=0 if full else 3, workload=args.workload)
             cpu = {"value": r["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
                    "sample": r["sample"]}
         except Exception as ex:  # reported, not fatal
             cpu = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
                    "sample": f"failed: {ex}"[:300]}
         try:
-            cpu_all = run_cpu_oracle_all_cores(args.cpu_seconds)
+            cpu_all = None if full else run_cpu_oracle_all_cores(args.cpu_seconds, args.workload)
         except Exception as ex:  # reported, not fatal
             cpu_all = {"value": None, "unit": UNIT, "cores": None, "kind": "oracle",
                        "sample": f"failed: {ex}"[:300]}
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "metric": METRICS[args.workload], "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": Wu, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "ctx": C, "window": Wn, "budget": N - 1,
+            "config": {"workload": wname, "ctx": C, "window": Wn, "budget": N - 1,
                        "heads": f"{hq}/{hkv}", "head_dim": D, "vocab": V, "logits": "bf16",
                        "kv": {"q4_0": "Q4_0", "f16": "F16"}[args.fmt]
                              + (", tree rows as cached" if args.tree_as_cache else ""),
                        "tree": "random depth<=16, planted path 8, p=0.8",
                        "l2": f"inputs > L2: {n_pool} step inputs x 7.4 MB and {n_rep} "
-                             f"KV-cache replicas cycled; L2 flushed (256 MB write) before "
-                             f"the timed replay",
+                             f"KV-cache replicas of {cap * row * 2 * hkv / 1e6:.0f} MB cycled; "
+                             f"L2 flushed (256 MB write) before the timed replay",
                        "graph": "one CUDA graph of K steps, replayed once untimed first"},
             "kv_logits_bytes_per_step": kv_b + lg_b,
             "kv_logits_gbs": kvlg_gbs,
@@ -616,21 +759,28 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(fmt="q4_0", tree_as_cache=False):
+def recorded_traffic(fmt="q4_0", tree_as_cache=False, workload=WORKLOAD):
     """DRAM bytes per step-kernel launch from the committed ncu summary, or
     None when the kernel sources changed since it was taken or the run is
-    not the one it was taken on (the Q4_0 cache, tree rows as given)."""
+    not the one it was taken on (the workload, the Q4_0 cache, tree rows as
+    given). The file holds one record per workload, each opened by its
+    ``workload:`` line."""
     if fmt != "q4_0" or tree_as_cache:
         return None
-    rec = {}
+    recs, cur = {}, None
     try:
         with open(os.path.join(ROOT, "profiles", "step_kernel_traffic.txt")) as f:
             for line in f:
                 if ":" in line and not line.startswith("#"):
                     k, v = line.split(":", 1)
-                    rec[k.strip()] = v.strip()
+                    k, v = k.strip(), v.strip()
+                    if k == "workload":
+                        cur = recs.setdefault(v, {})
+                    elif cur is not None:
+                        cur[k] = v
     except OSError:
         return None
+    rec = recs.get(workload, {})
     if rec.get("source_hash") != kernel_source_hash():
         return None
     try:
@@ -844,7 +994,11 @@ def main(argv=None):
         return
     if args.cpu_child:
         cpu_oracle_child(args.cpu_seconds, args.steps if not args.cpu_start_at else 10 ** 9,
-                         args.cpu_start_at, args.warmup if not args.cpu_start_at else 0)
+                         args.cpu_start_at, args.warmup if not args.cpu_start_at else 0,
+                         args.workload)
+        return
+    if args.oracle_replay:
+        oracle_replay(args.oracle_replay)
         return
     if args.impl == "reference":
         run_reference(args)
