@@ -72,6 +72,9 @@ def parse_args(argv=None):
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="long",
                     help="long: ctx 61440, window 2048 (the headline); full: ctx 131072, no "
                          "window (tensor-bound); short: ctx 4096, window 2048")
+    ap.add_argument("--accept-only", action="store_true",
+                    help="time the standalone dfv_greedy_accept (argmax + walk) alone over "
+                         "the workload's logits and print one JSON line")
     ap.add_argument("--oracle-replay", type=int, default=0, metavar="STEPS",
                     help="only time the oracle replaying STEPS chained steps of the long "
                          "workload (one thread) and print one JSON line")
@@ -122,6 +125,16 @@ def barrier(world):
 
 
 # ---------------------------------------------------------------- clocks
+
+def gpu_uuid(dev):
+    """The device's UUID as nvidia-smi names it, or None."""
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
 
 class ClockSampler:
     """nvidia-smi sampling of SM clock and throttle reasons while running."""
@@ -580,12 +593,7 @@ def run_gpu(args):
     g_warm = capture(Wu, 0)
     g_timed = capture(K, Wu)
 
-    gpu_id = None
-    try:
-        u = str(torch.cuda.get_device_properties(dev).uuid)
-        gpu_id = u if u.startswith("GPU-") else "GPU-" + u
-    except Exception:
-        gpu_id = None
+    gpu_id = gpu_uuid(dev)
     log = None
     if args.clock_log:
         log = f"{args.clock_log}.rank{rank}.csv" if world > 1 else args.clock_log
@@ -907,6 +915,71 @@ def run_e2e(args, api, cfg, steps_np, caches, ctx_all, ctx0, st, stream, dev):
                                       "in order"}
 
 
+def run_accept_only(args):
+    """dfv_greedy_accept alone: K calls over a pool of logits larger than L2
+    (one CUDA graph, replayed once untimed, L2 flushed, then timed with CUDA
+    events); the algorithmic bytes are the logits read."""
+    import numpy as np
+    import torch
+    from tree_verify_attention_gb300 import api, build
+    build.build()
+    cfg, wname = workload_cfg(args.workload)
+    dev = torch.device("cuda", 0)
+    N, V = cfg.n_nodes, cfg.vocab
+    K, Wu = args.steps, max(3, args.warmup)
+    from tree_verify_attention_gb300 import workload as W
+    steps_np = [W.make_step(cfg, i) for i in range(args.pool)]
+
+    def bf(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
+
+    lg = torch.stack([bf(s.logits) for s in steps_np]).to(dev)
+    par = torch.stack([torch.from_numpy(s.parent) for s in steps_np]).to(dev)
+    tok = torch.stack([torch.from_numpy(s.tokens) for s in steps_np]).to(dev)
+    am = torch.empty(N, dtype=torch.int32, device=dev)
+    acc = torch.empty(1, dtype=torch.int32, device=dev)
+    path = torch.empty(N, dtype=torch.int32, device=dev)
+    ot = torch.empty(N, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = api.workspace(api.accept_workspace_bytes(N, V), device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def one(i):
+        j = i % args.pool
+        api.greedy_accept(lg[j], par[j], tok[j], am, acc, path, ot, ws, status=status,
+                          stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(Wu):
+            one(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(K):
+            one(i)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    clocks = ClockSampler(gpu_uuid(dev), None)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        flush.zero_()
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    t = e0.elapsed_time(e1) / 1000.0 / K
+    nbytes = N * V * 2
+    hbm = _peaks().get("hbm_gbs") or 6800.0
+    print(json.dumps({"kernel": "accept_kernel<bf16>", "workload": wname, "calls": K,
+                      "us_per_call": t * 1e6, "logits_bytes": nbytes,
+                      "gbs": nbytes / t / 1e9, "frac_of_hbm": nbytes / t / 1e9 / hbm,
+                      "l2": f"{args.pool} logits sets of {nbytes / 1e6:.1f} MB cycled, L2 flushed "
+                            f"before the timed replay",
+                      "status": int(status.item()), "clocks": clk}), flush=True)
+
+
 def run_sweep(args):
     """Budget x tree-shape sweep on the 32768-context workload (window 2048,
     24/4 heads, D 256, vocabulary 151936 bf16, planted acceptance p = 0.8):
@@ -1005,6 +1078,9 @@ def main(argv=None):
         return
     if args.sweep:
         run_sweep(args)
+        return
+    if args.accept_only:
+        run_accept_only(args)
         return
     run_gpu(args)
 

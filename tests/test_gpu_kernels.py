@@ -198,6 +198,12 @@ def test_argmax_ties_and_edges(dtype):
     x[5, 0] = 9.0                                # max at the start
     x[6, 100000] = 7.0
     x[6, 99999] = 7.0
+    x[7] = -3.0                                  # negative maxima tied across chunks
+    x[7, 40000] = -2.5
+    x[7, 120000] = -2.5
+    x[8] = -1.0                                  # -0 and +0 in different chunks: 10000 wins
+    x[8, 30000] = 0.0
+    x[8, 10000] = -0.0
     parent = np.array([-1, 0, 0, 1, 1, 2, 5, 5, 0], np.int32)
     tokens = np.zeros(n, np.int32)
     logits = W.f32_to_bf16_bits(x) if dtype == "bf16" else x

@@ -8,19 +8,20 @@
 //
 // Design: the logits stream is HBM-bound (151936 x 23 bf16 = 7 MB per
 // step), so each (node, chunk) CTA streams its chunk with 16-byte loads,
-// all issued before any compare, and writes a (value, index) partial. The
-// last CTA to finish (atomic ticket in the workspace) merges the partials
-// per node and runs the walk in one warp: ballots pick the lowest matching
-// child. The ticket is reset by that CTA, so the workspace stays zeroed.
+// all issued before any compare, and folds its (value, index) maximum into
+// the node's 64-bit key with one atomic max (the packing makes the larger
+// key the larger value, then the lower index). The last CTA to finish
+// (atomic ticket in the workspace) exchanges each node's key for zero and
+// runs the walk in one warp: ballots pick the lowest matching child. Keys
+// and ticket end at zero, so the workspace stays zeroed.
 
 #include "common.cuh"
 #include "accept_impl.cuh"
 
 namespace dfv {
 
-size_t accept_workspace_bytes(int n_nodes, int vocab) {
-  const int chunks = accept_chunks(n_nodes, vocab);
-  return 256 + static_cast<size_t>(n_nodes) * chunks * sizeof(ArgPartial);
+size_t accept_workspace_bytes(int n_nodes, int /*vocab*/) {
+  return accept_scratch_bytes(n_nodes);
 }
 
 dfv_status accept_launch(int n_nodes, int vocab, int dtype, const void* logits,
@@ -49,7 +50,7 @@ dfv_status accept_launch(int n_nodes, int vocab, int dtype, const void* logits,
   p.path = path;
   p.out_tokens = out_tokens;
   p.ticket = reinterpret_cast<unsigned int*>(workspace);
-  p.partials = reinterpret_cast<ArgPartial*>(static_cast<char*>(workspace) + 256);
+  p.keys = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + kAcceptHeaderBytes);
   p.status = status;
   dim3 grid(chunks, n_nodes);
   if (dtype == DFV_DTYPE_BF16)

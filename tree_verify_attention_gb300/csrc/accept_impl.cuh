@@ -9,6 +9,7 @@ namespace dfv {
 
 constexpr int kAcceptThreads = 256;
 
+// A (value, index) argmax partial (the fused step's logits slices).
 struct ArgPartial {
   float v;
   int idx;
@@ -23,10 +24,16 @@ struct AcceptParams {
   int32_t* accept_len;
   int32_t* path;
   int32_t* out_tokens;
-  unsigned int* ticket;     // zero between launches
-  ArgPartial* partials;     // [n_nodes][chunks]
+  unsigned int* ticket;       // zero between launches
+  unsigned long long* keys;   // [n_nodes] packed (value, index) maxima; zero between launches
   uint32_t* status;
 };
+
+// Workspace: the ticket in the first 256 bytes, then one 8-byte key per node.
+constexpr size_t kAcceptHeaderBytes = 256;
+inline size_t accept_scratch_bytes(int n_nodes) {
+  return kAcceptHeaderBytes + ((static_cast<size_t>(n_nodes) * 8 + 255) & ~static_cast<size_t>(255));
+}
 
 // About four CTAs per SM over the whole grid, chunks of >= 2048 elements.
 inline int accept_chunks(int n_nodes, int vocab) {
@@ -46,6 +53,21 @@ inline int accept_chunk_len(int vocab, int chunks) {
 // and +0.0 compare equal, so the lower index wins between them.
 __device__ __forceinline__ bool beats(float v, int i, float w, int j) {
   return v > w || (v == w && i < j);
+}
+
+// (value, index) packed so that the larger key is the winner under
+// `beats`: the high word orders the floats (-0.0 taken as +0.0; every
+// non-NaN value gives a high word of at least 0x007FFFFF, so a real key is
+// above the zero a node's key starts from), the low word is ~index, larger
+// for the lower index.
+__device__ __forceinline__ unsigned long long arg_key(float v, int idx) {
+  uint32_t b = __float_as_uint(v == 0.f ? 0.f : v);
+  b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return (static_cast<unsigned long long>(b) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(idx));
+}
+
+__device__ __forceinline__ int key_index(unsigned long long k) {
+  return static_cast<int>(~static_cast<uint32_t>(k));
 }
 
 __device__ __forceinline__ void warp_argmax(float& v, int& i) {
@@ -141,41 +163,41 @@ __device__ __forceinline__ void chunk_argmax(const T* row, int begin, int end, f
   }
 }
 
-// Final per-node merge + walk, run by the last CTA. `s_am` receives the
+// The walk, run by the last CTA once every node's key is final: one thread
+// per node takes its key (and zeroes it for the next launch), then warp 0
+// walks the tree with ballots and writes the outputs. `s_am` receives the
 // argmax of every node.
 __device__ __forceinline__ void accept_tail(const AcceptParams& p, int* s_am, int* s_path) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int node = warp; node < p.n_nodes; node += kAcceptThreads / 32) {
-    float best = -INFINITY;
-    int bidx = INT_MAX;
-    for (int c = lane; c < p.chunks; c += 32) {
-      const ArgPartial* ap = p.partials + node * p.chunks + c;
-      const float v = __ldcg(&ap->v);
-      const int i = __ldcg(&ap->idx);
-      if (beats(v, i, best, bidx)) { best = v; bidx = i; }
+  // warp 0's tree loads go out first, beside the key exchanges below
+  int par[3], tok[3];
+  bool bad = false;
+  if (warp == 0) {
+#pragma unroll
+    for (int s = 0; s < 3; ++s) {
+      const int n = lane + 32 * s;
+      par[s] = -2;
+      tok[s] = 0;
+      if (n >= 1 && n < p.n_nodes) {
+        par[s] = p.parent[n];
+        tok[s] = p.tokens[n];
+      }
     }
-    warp_argmax(best, bidx);
-    if (lane == 0) {
-      s_am[node] = bidx;
-      p.argmax[node] = bidx;
-    }
+  }
+  for (int node = threadIdx.x; node < p.n_nodes; node += kAcceptThreads) {
+    const int am = key_index(atomicExch(p.keys + node, 0ull));
+    s_am[node] = am;
+    p.argmax[node] = am;
   }
   if (threadIdx.x == 0) *p.ticket = 0u;   // ready for the next launch
   __syncthreads();
   if (warp != 0) return;
-
-  int par[3], tok[3];
-  bool bad = false;
 #pragma unroll
   for (int s = 0; s < 3; ++s) {
     const int n = lane + 32 * s;
-    par[s] = -2;
-    tok[s] = 0;
-    if (n >= 1 && n < p.n_nodes) {
-      int pa = p.parent[n];
-      if (pa < 0 || pa >= n) { bad = true; pa = 0; }
-      par[s] = pa;
-      tok[s] = p.tokens[n];
+    if (n >= 1 && n < p.n_nodes && (par[s] < 0 || par[s] >= n)) {
+      bad = true;
+      par[s] = 0;
     }
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) report(p.status, DFV_DEV_BAD_TREE);
@@ -207,6 +229,9 @@ __device__ __forceinline__ void accept_tail(const AcceptParams& p, int* s_am, in
   if (lane == 0) *p.accept_len = L;
 }
 
+// One CTA per (chunk, node): the chunk's argmax goes into the node's key by
+// a 64-bit atomic max, then a ticket (release / acquire) counts the CTAs;
+// the last one takes the keys and walks. No CTA waits for another.
 template <typename T>
 __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(AcceptParams p) {
   __shared__ int s_am[kMaxNodes];
@@ -221,16 +246,14 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(AcceptParams p) 
   chunk_argmax<T>(row, begin, end, best, bidx);
   block_argmax(best, bidx);
   if (threadIdx.x == 0) {
-    ArgPartial* ap = p.partials + node * p.chunks + chunk;
-    ap->v = best;
-    ap->idx = bidx;
-    __threadfence();
+    atomicMax(p.keys + node, arg_key(best, bidx));
     const unsigned total = gridDim.x * gridDim.y;
-    s_last = (atomicAdd(p.ticket, 1u) == total - 1);
+    unsigned int old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p.ticket) : "memory");
+    s_last = old == total - 1;
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   accept_tail(p, s_am, s_path);
 }
 

@@ -72,9 +72,9 @@ extern "C" dfv_status dfv_greedy_accept_static(int n_nodes, int vocab, int logit
   void* scratch = scratch_for_current_device();
   if (scratch == nullptr) return DFV_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The array keeps whatever the previous call left; the ticket must start at
-  // zero, so clear it in stream order before the kernel.
-  if (cudaMemsetAsync(scratch, 0, 256, s) != cudaSuccess) return DFV_ERR_CUDA;
+  // The array keeps whatever the previous call left; the ticket and the keys
+  // must start at zero, so clear them in stream order before the kernel.
+  if (cudaMemsetAsync(scratch, 0, accept_scratch_bytes(n_nodes), s) != cudaSuccess) return DFV_ERR_CUDA;
   const int chunks = accept_chunks(n_nodes, vocab);
   AcceptParams p;
   p.n_nodes = n_nodes;
@@ -89,7 +89,7 @@ extern "C" dfv_status dfv_greedy_accept_static(int n_nodes, int vocab, int logit
   p.path = path;
   p.out_tokens = out_tokens;
   p.ticket = reinterpret_cast<unsigned int*>(scratch);
-  p.partials = reinterpret_cast<ArgPartial*>(static_cast<char*>(scratch) + 256);
+  p.keys = reinterpret_cast<unsigned long long*>(static_cast<char*>(scratch) + kAcceptHeaderBytes);
   p.status = status;
   dim3 grid(chunks, n_nodes);
   if (logits_dtype == DFV_DTYPE_BF16)
