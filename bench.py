@@ -89,6 +89,10 @@ def parse_args(argv=None):
                     help="attend the tree rows as the commit stores them")
     ap.add_argument("--sweep", action="store_true",
                     help="budget x tree-shape sweep at context 32768 (one JSON line per point)")
+    ap.add_argument("--sweep-out", default=None,
+                    help="write the sweep's table (budget.py's selector reads it) to this file")
+    ap.add_argument("--sweep-steps", type=int, default=64, help="timed steps per sweep point")
+    ap.add_argument("--sweep-inputs", type=int, default=4, help="step inputs per sweep point")
     return ap.parse_args(argv)
 
 
@@ -980,84 +984,72 @@ def run_accept_only(args):
                       "status": int(status.item()), "clocks": clk}), flush=True)
 
 
+def _sweep_inputs(job):
+    """Step inputs of one sweep point (runs in a spawned worker)."""
+    from tree_verify_attention_gb300 import workload as W
+    name, n = job
+    cfg = {c.name: c for c in W.sweep_configs()}[name]
+    return [W.make_step(cfg, i) for i in range(n)]
+
+
 def run_sweep(args):
     """Budget x tree-shape sweep on the 32768-context workload (window 2048,
-    24/4 heads, D 256, vocabulary 151936 bf16, planted acceptance p = 0.8):
-    per point, GPU steps/s over a CUDA graph of strictly serial steps (inputs
-    cycled over 16 step inputs and 16 cache replicas), the mean accept length
-    of those inputs (the greedy walk of the oracle, which the kernel matches
-    bit for bit) and their product, accepted tokens/s. The pages found budget
-    22 the best trade-off on an RTX 3090 ("We got 207 tok/s ...", DFlash
-    section); this measures where it lies on this GPU."""
-    import numpy as np
+    24/4 heads, D 256, vocabulary 151936 bf16, Q4_0 cache): every point of
+    the sweep (budgets 0, 8, 22, 48, 64; chain, 2-ary, 4-ary and random
+    trees; planted acceptance p = 0.5, 0.8, 0.95; seeds 0-4), each timed
+    over a CUDA graph of strictly serial steps with the accept lengths read
+    back from the kernel (budget.SweepBench). One JSON line per point, then
+    a summary line; --sweep-out also writes the table that budget.py's
+    selector reads. The pages found budget 22 the best trade-off on an
+    RTX 3090 ("We got 207 tok/s ...", DFlash section); this measures the
+    step-cost side of that trade-off on this GPU."""
+    import multiprocessing as mp
     import torch
-    import oracle
-    from tree_verify_attention_gb300 import api, build
+    from tree_verify_attention_gb300 import budget, build
     from tree_verify_attention_gb300 import workload as W
-    build.build()
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    points = [c for c in W.sweep_configs() if c.p_accept == 0.8 and c.seed == 0]
-    K, R, P = max(64, args.steps // 5), 16, 16
-    base_cfg = points[0]
-    C, hkv, hq, D, Wn, V = (base_cfg.ctx_len, base_cfg.n_kv_heads, base_cfg.n_q_heads,
-                            base_cfg.head_dim, base_cfg.window, base_cfg.vocab)
-    cap = C + (K // R + 2) * 65                 # room for every step's commit (N <= 65)
-    kf, vf = W.make_context(base_cfg)
-    base = api.KVCache(hkv, D, cap, device=dev, fmt=args.fmt)
-    base.fill(torch.from_numpy(kf).to(dev), torch.from_numpy(vf).to(dev))
-    del kf, vf
-    k_all = base.k.unsqueeze(0).repeat(R, 1, 1, 1)
-    v_all = base.v.unsqueeze(0).repeat(R, 1, 1, 1)
-    ctx0 = torch.full((R,), C, dtype=torch.int32, device=dev)
-    ctx_all = ctx0.clone()
-    caches = [CacheView(k_all[r], v_all[r], ctx_all[r:r + 1], hkv, D, cap, args.fmt) for r in range(R)]
-    stream = torch.cuda.Stream(device=dev)
-
-    def bf(x):
-        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(dev)
-
-    for cfg in points:
-        N = cfg.n_nodes
-        pool = [W.make_step(cfg, i) for i in range(P)]
-        ins = [(bf(s.q), bf(s.k_tree), bf(s.v_tree), torch.from_numpy(s.parent).to(dev),
-                torch.from_numpy(s.tokens).to(dev), bf(s.logits)) for s in pool]
-        st = api.VerifyStep(N, hq, hkv, D, Wn, cap, V, max_depth=max(cfg.max_depth, 1), device=dev)
-        lens = []
-        for s in pool:
-            am = oracle.accept.node_argmax(W.bf16_bits_to_f32(s.logits))
-            lens.append(len(oracle.accept.greedy_walk(s.parent, s.tokens, am)[0]))
-
-        def one(i):
-            st.run(caches[i % R], *ins[i % P], stream=stream, tree_as_cache=args.tree_as_cache)
-
-        with torch.cuda.stream(stream):
-            for i in range(4):
-                one(i)
-            ctx_all.copy_(ctx0)
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(K):
-                one(i)
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                ctx_all.copy_(ctx0)
-                g.replay()
-            ctx_all.copy_(ctx0)
-            ev0.record(stream)
-            g.replay()
-            ev1.record(stream)
-        torch.cuda.synchronize()
-        sps = K / (ev0.elapsed_time(ev1) / 1000.0)
-        mean_l = float(np.mean(lens))
-        print(json.dumps({"sweep": cfg.name, "budget": cfg.budget, "tree": cfg.tree, "p_accept": 0.8,
-                          "ctx": C, "window": Wn, "kv": args.fmt, "steps_per_s": sps,
-                          "us_per_step": 1e6 / sps, "mean_accept_len": mean_l,
-                          "accepted_tokens_per_s": sps * mean_l,
-                          "device_status": int(st.status.item())}), flush=True)
-        del g, st, ins
+    points = W.sweep_configs()
+    n_in = args.sweep_inputs
+    # input generation in spawned workers, a batch ahead of the GPU
+    ctx = mp.get_context("spawn")
+    workers = max(1, min(16, len(os.sched_getaffinity(0)) - 1))
+    with ctx.Pool(workers) as pool:
+        build.build()
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        K = args.sweep_steps
+        sb = budget.SweepBench(points[0], replicas=8, steps=K, device=dev, fmt=args.fmt,
+                               max_nodes=max(c.n_nodes for c in points))
+        clocks = ClockSampler(gpu_uuid(dev), args.clock_log)
+        clocks.start()
+        recs = []
+        t0 = time.time()
+        batch = 24
+        jobs = [(c.name, n_in) for c in points]
+        pending = pool.map_async(_sweep_inputs, jobs[:batch])
+        for b0 in range(0, len(points), batch):
+            xs_batch = pending.get()
+            if b0 + batch < len(points):
+                pending = pool.map_async(_sweep_inputs, jobs[b0 + batch:b0 + 2 * batch])
+            for cfg, xs in zip(points[b0:b0 + batch], xs_batch):
+                us, lens = sb.time_point(cfg, xs)
+                rec = budget.point_record(cfg, us, lens)
+                recs.append(rec)
+                print(json.dumps({"sweep": cfg.name, **rec, "ctx": cfg.ctx_len,
+                                  "window": cfg.window, "kv": args.fmt,
+                                  "mean_accept_len": sum(lens) / len(lens),
+                                  "accepted_tokens_per_s": 1e6 / us * sum(lens) / len(lens)}),
+                      flush=True)
+        clk = clocks.stop()
+    meta = budget.table_meta(points[0], K, 8, args.fmt)
+    meta.update({"clocks": clk, "inputs_per_point": n_in, "seconds": time.time() - t0,
+                 "command": "python bench.py --sweep --sweep-out "
+                            "tree_verify_attention_gb300/budget_table_gb300.json"})
+    table = {"meta": meta, "points": recs}
+    if args.sweep_out:
+        budget.write_table(table, args.sweep_out)
+    best = {p: budget.select_budget(p, table) for p in (0.5, 0.8, 0.95)}
+    print(json.dumps({"sweep_summary": len(recs), "clocks": clk,
+                      "best": {str(p): vars(c) for p, c in best.items()}}), flush=True)
 
 
 def main(argv=None):

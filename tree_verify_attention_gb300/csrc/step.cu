@@ -59,7 +59,10 @@ constexpr int kMaxStepSplits = 256;
 constexpr int kMaxStepGrid = 256;   // CTAs of one launch at most
 constexpr int kMaxStagedSlices = 8; // logits slices one CTA stages at most
 constexpr long kSliceCostBytes = 65536;  // per-slice scan overhead (a CTA-wide reduction), in bytes of streaming
-constexpr int kLongSpares = 8;      // CTAs left to the logits when the attention could use every SM
+// the launch planner's cost model (see step_plan): a unit's key chunk, and
+// the logits bytes a spare CTA stages and scans per microsecond
+constexpr long kChunkCostNs = 6000;
+constexpr long kSpareBytesPerUs = 32000;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kLogitVecs = 16;      // 16-byte logits vectors a thread keeps in flight
 
@@ -1360,9 +1363,27 @@ static bool step_plan(int n_nodes, int hq, int hkv, int head_dim, int window, in
   long s;
   if (groups * tb <= pl->grid - (with_accept ? 1 : 0)) {
     s = tb;
+  } else if (!with_accept) {
+    s = pl->grid / groups;
   } else {
-    const long keep = with_accept ? (kLongSpares < pl->grid - groups ? kLongSpares : pl->grid - groups) : 0;
-    s = (pl->grid - keep) / groups;
+    // Keep `keep` CTAs out of the attention (the walker and keep - 1 that
+    // scan the logits): the count that minimises the longer of the two
+    // estimated paths, a unit's chunks at kChunkCostNs each and a spare's
+    // share of the logits at kSpareBytesPerUs (both measured on a GB300
+    // over budgets 22 to 64); ties go to the fewer spares.
+    const long lbytes = static_cast<long>(n_nodes) * vocab * (logits_dtype == DFV_DTYPE_BF16 ? 2 : 4);
+    long best = -1, best_cost = 0;
+    for (long keep = 2; keep <= pl->grid - groups; ++keep) {
+      const long sk = (pl->grid - keep) / groups;
+      const long attn = (tb + sk - 1) / sk * kChunkCostNs;
+      const long lg = lbytes * 1000 / ((keep - 1) * kSpareBytesPerUs);
+      const long cost = attn > lg ? attn : lg;
+      if (best < 0 || cost < best_cost) {
+        best = keep;
+        best_cost = cost;
+      }
+    }
+    s = (pl->grid - best) / groups;
   }
   if (s > kMaxStepSplits) s = kMaxStepSplits;
   {
