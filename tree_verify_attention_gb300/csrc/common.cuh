@@ -41,6 +41,15 @@ __device__ __forceinline__ bool wait_bounded(F done) {
   return false;
 }
 
+// Named CTA barrier `id` (1..15) over `count` threads (a multiple of 32):
+// sync waits for all of them, arrive counts this thread without waiting.
+__device__ __forceinline__ void named_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void report(uint32_t* status, uint32_t bits) {
   if (status != nullptr) atomicOr(status, bits);
 }

@@ -26,10 +26,14 @@
 //     copied as they are) into 128-byte-swizzled smem; S = Q K^T by
 //     tcgen05.mma into TMEM (M = 128 rows, N = 128 keys, K = D); four
 //     threads per row read S from TMEM, mask (window, ancestors), exchange
-//     the row max, exp2, write P (fp16); O += P V by tcgen05.mma (M = 128,
-//     N = D, K = 128 keys; V as an MN-major operand). The running max only
-//     moves (O rescaled in TMEM) when a chunk's max exceeds it by more than
-//     2^8, so P <= 256 fits fp16;
+//     the row max, exp2, write P (fp16) back into TMEM over S; O += P V by
+//     tcgen05.mma with P from TMEM (M = 128, N = D, K = 128 keys; V as an
+//     MN-major operand). The running max only moves (O rescaled in TMEM)
+//     when a chunk's max exceeds it by more than 2^8, so P <= 256 fits fp16.
+//     A unit with several chunks pipelines them: the next chunk's raw rows
+//     are copied during the softmax, its K is decoded and its S (into a
+//     second TMEM buffer) issued while P V runs, and its V decoded once P V
+//     is done;
 //   * each split writes its normalised O rows (fp16) with their max and sum
 //     to the workspace (one bulk copy) and marks its ready word; the splits
 //     of a group wait for one another (time-bounded waits) and each merges a
@@ -128,7 +132,7 @@ struct StepSmem {
   static constexpr bool kBulk = (kRowB % 16) == 0;
   static constexpr int kTileB = kRowsPerTile * D * 2;        // one [128][D] fp16 tile
   static constexpr int kQ = 0;                               // Q of the tile
-  static constexpr int kK = kQ + kTileB;                     // K^, then P
+  static constexpr int kK = kQ + kTileB;                     // K^
   static constexpr int kKBytes0 = kChunk * D * 2;
   static constexpr int kKBytes1 = kChunk * kChunk * 2;
   static constexpr int kKBytes = kKBytes0 > kKBytes1 ? kKBytes0 : kKBytes1;
@@ -136,7 +140,12 @@ struct StepSmem {
   static constexpr int kRawK = kChunk * D * 2 - 2 * kChunk * kRowB;   // raw K's offset in sV
   static constexpr int kRawV = kRawK + kChunk * kRowB;                // raw V's offset in sV
   static constexpr int kQStage = kK;                         // bf16 Q rows land here (sK, then sV)
-  static constexpr int kBars = kV + kChunk * D * 2;
+  // raw K / V of a unit's later chunks, copied while the chunk before is
+  // still in its softmax and P V: raw K in sK (free once S of that chunk is
+  // done; P is in TMEM), raw V in a region of its own
+  static constexpr int kRawK2 = kKBytes1;                    // offset in sK
+  static constexpr int kRawV2 = kV + kChunk * D * 2;
+  static constexpr int kBars = kRawV2 + (kBulk ? kChunk * kRowB : 0);
   static constexpr int kSpareStageBytes = kBars;             // logits staging of a CTA without a unit
   // logits staging of a unit whose tile has at most kLightRows real rows:
   // past its staged Q rows, up to the raw K / V (free until the dequant)
@@ -147,6 +156,8 @@ struct StepSmem {
   static_assert(kRawK % 16 == 0 && kRawV % 16 == 0, "bulk-copy destinations 16-byte aligned");
   static_assert(kRowsPerTile * D * 2 <= kKBytes + kRawK, "staged Q rows stay clear of raw K / V");
   static_assert(kRowsPerTile * (D * 2 + 16) <= kV, "epilogue staging fits in sQ + sK");
+  static_assert(!kBulk || kRawK2 + kChunk * kRowB <= kKBytes, "next raw K fits in sK");
+  static_assert(kRawK2 % 16 == 0 && kRawV2 % 16 == 0, "bulk-copy destinations 16-byte aligned");
 };
 
 // ---------------------------------------------------------------- small helpers
@@ -572,6 +583,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
   uint64_t* bar_lg2 = bar_kv + 3;
   uint64_t* bar_q = bar_kv + 4;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_kv + 5);
+  uint64_t* bar_s = bar_kv + 6;      // S of a chunk done
 
   __shared__ int s_J[kMaxNodes], s_dep[kMaxNodes];
   __shared__ uint32_t s_anc[kMaxNodes][kMaskWords];
@@ -623,17 +635,19 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     }
   };
 
-  auto issue_kv = [&](int cc) {
-    // raw K -> sV, raw V -> sV + kRawV (both read into registers before V^
-    // is written over them)
+  // raw K / V of chunk cc -> dk / dv (read into registers before K^ / V^
+  // are written over them); thread 0 counts the copies not yet waited for
+  int kv_pending = 0;
+  auto issue_kv = [&](int cc, uint8_t* dk, uint8_t* dv) {
     const int j0 = lo_min + cc * kChunk;
     const int nk = min(kChunk, C - j0);
     const uint32_t bytes = static_cast<uint32_t>(nk * L::kRowB);
     const size_t off = (static_cast<size_t>(h) * p.capacity + j0) * L::kRowB;
     fence_proxy_async_smem();
     mbar_arrive_expect_tx(bar_kv, 2 * bytes);
-    bulk_g2s(sV + L::kRawK, p.k_cache + off, bytes, bar_kv);
-    bulk_g2s(sV + L::kRawV, p.v_cache + off, bytes, bar_kv);
+    bulk_g2s(dk, p.k_cache + off, bytes, bar_kv);
+    bulk_g2s(dv, p.v_cache + off, bytes, bar_kv);
+    ++kv_pending;
   };
   // the tile's rows [128 grp, 128 grp + rows_g): node n's query heads of KV
   // head h are contiguous, so one bulk copy per node lands the bf16 rows in
@@ -690,7 +704,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     s_C = C;
     derive();
     if constexpr (L::kBulk && kQ4) {
-      if (first_kv) issue_kv(c0);
+      if (first_kv) issue_kv(c0, sV + L::kRawK, sV + L::kRawV);
     }
   };
   // Warp 0 first, before any load of its own (the barrier-init fence would
@@ -708,6 +722,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       mbar_init(bar_mma, 1);
       mbar_init(bar_lg, 1);
       mbar_init(bar_q, 1);
+      mbar_init(bar_s, 1);
       mbar_init(bar_lg2, 1);
       fence_mbar_init();
       if (!p.pipelined) ctx_and_first_kv();
@@ -893,98 +908,134 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     tc::fence_after_sync();
 
     const uint32_t tmem = *s_tmem;
-    const uint32_t t_s = tmem;                    // S: columns [0, 128)
     const uint32_t t_o = tmem + kChunk;           // O: columns [128, 128 + D)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int r = (warp & 3) * 32 + lane;   // this thread's row
     const int hc = warp >> 2;               // its quarter of the keys / of O's columns
     // A warp whose 32 rows all lie past the last row (a padded tile) skips
-    // the second half of the softmax and the epilogue: its P rows keep the
-    // finite operand values under them, and its O rows reach no output.
+    // the second half of the softmax and the epilogue: its P rows are zero,
+    // and its O rows reach no output.
     const bool live = grp * kRowsPerTile + (warp & 3) * 32 < p.rows;
-    uint32_t ph_kv = 0, ph_mma = 0;
+    uint32_t ph_kv = 0, ph_s = 0, ph_pv = 0;
+    int s_pend = 0, pv_pend = 0;   // thread 0: MMA batches issued, not yet waited for
     float m_run = -INFINITY, l_half = 0.f;
     bool o_valid = false, alive = true;
     const float sc = p.scale_log2;
+    const int n_it = c1 - c0;
+    auto chunk_of = [&](int i) { return i < n_tree ? T - 1 : c0 + (i - n_tree); };
+    // S of chunk i in TMEM columns [0, 128) or [384, 512) by parity (clear
+    // of O); its P (fp16 pairs) overwrites the first 64 of them
+    auto t_sbuf = [&](int i) { return tmem + ((i & 1) ? 384u : 0u); };
 
+    // One operand of a committed chunk at key j0 (nk keys) into its swizzled
+    // [keys][D] fp16 tile (kvi 0: K^ -> sK, 1: V^ -> sV).
+    // binary16 rows: each thread copies 16-byte pieces straight into their
+    // swizzled slots; rows past the chunk's keys are zero
+    // (threads t0, t0 + 1, ... of nt take the pieces in turn)
+    auto f16_copy = [&](int kvi, int j0, int nk, int t0, int nt) {
+      constexpr int PR = D / 8;                           // pieces per row
+      const uint8_t* b = (kvi ? p.v_cache : p.k_cache) + (static_cast<size_t>(h) * p.capacity + j0) * (D * 2);
+      uint8_t* dst0 = kvi ? sV : sK;
 #pragma unroll 1
-    for (int i = 0; i < c1 - c0 && alive; ++i) {
-      const int cc = i < n_tree ? T - 1 : c0 + (i - n_tree);
+      for (int it = t0; it < kChunk * PR; it += nt) {
+        const int key = it / PR, c = it % PR;
+        uint8_t* dst = dst0 + tc::sw128_offset(key, c, kChunk);
+        if (key < nk) cp_async16(dst, b + key * (D * 2) + c * 16);
+        else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      cp_async_wait_all();
+    };
+    // Q4_0 rows: a work item is a pair of blocks (36 bytes = 9 words, 64
+    // elements = one swizzle block) of one key row. Within a warp, lanes
+    // 8i..8i+7 take eight consecutive keys of the same pair: the 16-byte
+    // stores of each 8-lane phase then fall on 8 distinct swizzled granules,
+    // and the 9-word loads (word stride 9 * pairs-per-row between keys, 9
+    // between pairs) fall on 32 distinct banks. `raw` is the rows' copy in
+    // smem, or null to read them from the cache.
+    // Item g (< HALF) of an operand; the thread of item g holds lane g % 32.
+    constexpr int PPK = D / 64;                           // block pairs per key row
+    constexpr int HALF = kChunk * PPK;                    // items per operand
+    constexpr int kWorkers = kStepThreads - 32;           // warps 1.. (warp 0 issues the MMAs)
+    static_assert(HALF <= 2 * kWorkers, "at most two dequant items per worker and operand");
+    auto q4_pos = [&](int g, int& key, int& pp) {
+      const int l = g & 31;
+      key = (g >> 5) * (32 / PPK) + (l & 7) + 8 * (l / (8 * PPK));
+      pp = (l >> 3) % PPK;
+    };
+    auto q4_load = [&](int g, int kvi, const uint8_t* raw, int j0, int nk, uint32_t* w) {
+      int key, pp;
+      q4_pos(g, key, pp);
+      const bool on = g < HALF && key < nk;
+      const uint8_t* base = raw != nullptr ? raw
+          : (kvi ? p.v_cache : p.k_cache) + (static_cast<size_t>(h) * p.capacity + j0) * L::kRowB;
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(base + (on ? key * L::kRowB + pp * 36 : 0));
+#pragma unroll
+      for (int e = 0; e < 9; ++e) w[e] = on ? src[e] : 0u;
+    };
+    auto q4_store = [&](int g, int kvi, const uint32_t* w) {
+      if (g < HALF) {
+        int key, pp;
+        q4_pos(g, key, pp);
+        uint4 o4[8];
+        q4_0_pair_chunks(w, o4);       // all-zero blocks dequantise to zeros
+        uint8_t* dst = kvi ? sV : sK;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          *reinterpret_cast<uint4*>(dst + tc::sw128_offset(key, pp * 8 + e, kChunk)) = o4[e];
+      }
+    };
+    // a wait of the workers alone: thread 32 polls, the workers meet
+    __shared__ int s_wok;
+    auto worker_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      if (tid == 32) {
+        const bool ok = mbar_wait_bounded(bar, parity);
+        if (!ok) report(p.status, DFV_DEV_TIMEOUT);
+        s_wok = ok ? 1 : 0;
+      }
+      named_sync(1, kWorkers);
+      return s_wok != 0;
+    };
+    auto kv_wait = [&]() -> bool {
+      if (!cta_wait(bar_kv, ph_kv, &s_ok, p.status)) return false;
+      ph_kv ^= 1u;
+      kv_pending = 0;
+      return true;
+    };
+    // S = Q K^T (M = 128 rows, N = 128 keys, K = D) into t_dst
+    auto issue_s = [&](uint32_t t_dst) {
+      tc::fence_after_sync();
+      const uint32_t ida = tc::idesc_f16(kRowsPerTile, kChunk);
+      const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK);
+#pragma unroll 1
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = static_cast<uint32_t>((kk >> 2) * kRowsPerTile * 128 + (kk & 3) * 32);
+        tc::mma_f16(t_dst, tc::smem_desc_sw128(qa + off, 1024), tc::smem_desc_sw128(ka + off, 1024), ida,
+                    kk > 0 ? 1u : 0u);
+      }
+      tc::commit(bar_s);
+      ++s_pend;
+    };
+
+    // ---- the first chunk: K^ and V^ together, then its S. Its raw rows
+    // (Q4_0, bulk) were copied into sV at entry; the tree chunk is built
+    // from the tree rows.
+    if (n_it > 0) {
+      const int cc = chunk_of(0);
       const bool committed = cc < n_cc;
       const int j0 = lo_min + cc * kChunk;
       const int nk = committed ? min(kChunk, C - j0) : 0;
       if (committed && !kQ4) {
-        // binary16 cache rows are MMA operands as they are: each thread copies
-        // its 16-byte pieces of the K and V rows straight into their
-        // swizzled slots; rows past the chunk's keys are zero
-        constexpr int PR = D / 8;                         // pieces per row
-        const uint8_t* kb = p.k_cache + (static_cast<size_t>(h) * p.capacity + j0) * (D * 2);
-        const uint8_t* vb = p.v_cache + (static_cast<size_t>(h) * p.capacity + j0) * (D * 2);
-#pragma unroll 1
-        for (int it = tid; it < 2 * kChunk * PR; it += kStepThreads) {
-          const int kvi = it / (kChunk * PR), rem = it % (kChunk * PR);
-          const int key = rem / PR, c = rem % PR;
-          uint8_t* dst = (kvi ? sV : sK) + tc::sw128_offset(key, c, kChunk);
-          if (key < nk) cp_async16(dst, (kvi ? vb : kb) + key * (D * 2) + c * 16);
-          else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-        }
-        cp_async_wait_all();
+        f16_copy(0, j0, nk, tid, kStepThreads);
+        f16_copy(1, j0, nk, tid, kStepThreads);
       } else if (committed) {
-        if constexpr (L::kBulk) {
-          if (tid == 0 && !(i == 0 && first_kv)) issue_kv(cc);
-          if (!cta_wait(bar_kv, ph_kv, &s_ok, p.status)) { alive = false; break; }
-          ph_kv ^= 1u;
-        }
-        // K: raw -> sK, V: raw -> sV, both [keys][D] swizzled. A work item is
-        // a pair of Q4_0 blocks (36 bytes = 9 words, 64 elements = one
-        // swizzle block) of one key row. Within a warp, lanes 8i..8i+7 take
-        // eight consecutive keys of the same pair: the 16-byte stores of each
-        // 8-lane phase then fall on 8 distinct swizzled granules, and the
-        // 9-word loads (word stride 9 * pairs-per-row between keys, 9 between
-        // pairs) fall on 32 distinct banks. Every raw word (staged in sV) is
-        // loaded before the barrier, so the raw rows are consumed before V^
-        // overwrites them; the decode is one loop body for both items.
-        {
-          constexpr int PPK = D / 64;                     // block pairs per key row
-          constexpr int HALF = kChunk * PPK;              // items per operand
-          constexpr int IPT = (2 * HALF + kStepThreads - 1) / kStepThreads;
-          static_assert(IPT <= 2, "at most two dequant items per thread");
-          auto item = [&](int u, int& kvi, int& key, int& pp) {
-            const int g = tid + u * kStepThreads;
-            kvi = g / HALF;
-            const int rem = g % HALF, l = rem & 31;
-            key = (rem >> 5) * (32 / PPK) + (l & 7) + 8 * (l / (8 * PPK));
-            pp = (l >> 3) % PPK;
-            return g < 2 * HALF;
-          };
-          uint32_t w0[9], w1[9];
-          auto load = [&](int u, uint32_t* w) {
-            int kvi, key, pp;
-            const bool on = item(u, kvi, key, pp) && key < nk;
-            const uint8_t* base;
-            if constexpr (L::kBulk) base = sV + (kvi ? L::kRawV : L::kRawK);
-            else base = (kvi ? p.v_cache : p.k_cache) + (static_cast<size_t>(h) * p.capacity + j0) * L::kRowB;
-            const uint32_t* src = reinterpret_cast<const uint32_t*>(base + (on ? key * L::kRowB + pp * 36 : 0));
-#pragma unroll
-            for (int e = 0; e < 9; ++e) w[e] = on ? src[e] : 0u;
-          };
-          load(0, w0);
-          if (IPT > 1) load(1, w1);
+        if constexpr (L::kBulk) alive = kv_wait();
+        if (alive) {
+          uint32_t wk[9], wv[9];
+          q4_load(tid, 0, L::kBulk ? sV + L::kRawK : nullptr, j0, nk, wk);
+          q4_load(tid, 1, L::kBulk ? sV + L::kRawV : nullptr, j0, nk, wv);
           if constexpr (L::kBulk) __syncthreads();   // raw rows (in sV) consumed
-#pragma unroll 1
-          for (int u = 0; u < IPT; ++u) {
-            int kvi, key, pp;
-            if (item(u, kvi, key, pp)) {
-              uint4 o4[8];
-              q4_0_pair_chunks(w0, o4);       // all-zero blocks dequantise to zeros
-              uint8_t* dst = kvi ? sV : sK;
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                *reinterpret_cast<uint4*>(dst + tc::sw128_offset(key, pp * 8 + e, kChunk)) = o4[e];
-            }
-#pragma unroll
-            for (int e = 0; e < 9; ++e) w0[e] = w1[e];
-          }
+          q4_store(tid, 0, wk);
+          q4_store(tid, 1, wv);
         }
       } else {
         // tree chunk: keys t = 0..N-1 from tree_k / tree_v (bf16 -> fp16);
@@ -1053,30 +1104,36 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       }
       fence_proxy_async_smem();
       __syncthreads();
+      if (alive && tid == 0) issue_s(t_sbuf(0));
+    }
 
-      // ---- S = Q K^T (M = 128 rows, N = 128 keys, K = D)
-      if (tid == 0) {
-        tc::fence_after_sync();
-        const uint32_t ida = tc::idesc_f16(kRowsPerTile, kChunk);
-        const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK);
+    // ---- chunk i: its S is in flight. Softmax -> P (TMEM); P V(i) goes in
+    // flight and, under it, K^ of chunk i + 1 is built and its S issued;
+    // once P V(i) is done, V^ of chunk i + 1. The raw rows of chunk i + 1
+    // are copied while chunk i's softmax runs.
 #pragma unroll 1
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = static_cast<uint32_t>((kk >> 2) * kRowsPerTile * 128 + (kk & 3) * 32);
-          tc::mma_f16(t_s, tc::smem_desc_sw128(qa + off, 1024), tc::smem_desc_sw128(ka + off, 1024), ida,
-                      kk > 0 ? 1u : 0u);
-        }
-        tc::commit(bar_mma);
-      }
-      if (!cta_wait(bar_mma, ph_mma, &s_ok, p.status)) { alive = false; break; }
-      ph_mma ^= 1u;
+    for (int i = 0; i < n_it && alive; ++i) {
+      const int cc = chunk_of(i);
+      const bool committed = cc < n_cc;
+      const int j0 = lo_min + cc * kChunk;
+      const int nk = committed ? min(kChunk, C - j0) : 0;
+      const uint32_t t_sb = t_sbuf(i);
+      if (!cta_wait(bar_s, ph_s, &s_ok, p.status)) { alive = false; break; }
+      ph_s ^= 1u;
+      s_pend = 0;
       tc::fence_after_sync();
+      // K^ is consumed: the next chunk's raw K / V go in flight (every chunk
+      // after the first is committed)
+      if constexpr (L::kBulk && kQ4) {
+        if (tid == 0 && i + 1 < n_it) issue_kv(chunk_of(i + 1), sK + L::kRawK2, smem + L::kRawV2);
+      }
 
       // ---- masked softmax of the 128-row tile: four threads per row, 32
       // keys each, loaded from TMEM once
       {
         const int kb0 = hc * 32;
         float s[32];
-        tc::ld32(t_s + lane_base + kb0, s);
+        tc::ld32(t_sb + lane_base + kb0, s);
         const int node = s_row_node[r], lo = s_row_lo[r];
         float cm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (committed) {
@@ -1114,20 +1171,18 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
             m_run = cmax;
           }
           const float sub = m_run == -INFINITY ? 0.f : m_run;
+          // P of this thread's 32 keys as 16 fp16 pairs over its S columns
+          // (every S load of the tile precedes the barrier above)
           float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+          uint32_t pw[16];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t w4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float p0 = tc::ex2(s[c * 8 + 2 * e] - sub);
-              const float p1 = tc::ex2(s[c * 8 + 2 * e + 1] - sub);
-              rs4[e] += p0 + p1;
-              w4[e] = pack_half2(p0, p1);
-            }
-            *reinterpret_cast<uint4*>(sK + tc::sw128_offset(r, hc * 4 + c, kRowsPerTile)) =
-                make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          for (int k2 = 0; k2 < 16; ++k2) {
+            const float p0 = tc::ex2(s[2 * k2] - sub);
+            const float p1 = tc::ex2(s[2 * k2 + 1] - sub);
+            rs4[k2 & 3] += p0 + p1;
+            pw[k2] = pack_half2(p0, p1);
           }
+          tc::st16(t_sb + lane_base + hc * 16, pw);
           l_half = l_half * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
           if (o_valid && __any_sync(0xffffffffu, rescale)) {
             // this warp's quarter of the row's O columns
@@ -1141,32 +1196,107 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
               tc::st8(t_o + lane_base + col, ov);
             }
           }
+        } else {
+          // rows past the last: zero P (their O rows reach no output)
+          uint32_t pw[16];
+#pragma unroll
+          for (int k2 = 0; k2 < 16; ++k2) pw[k2] = 0u;
+          tc::st16(t_sb + lane_base + hc * 16, pw);
         }
       }
-      fence_proxy_async_smem();
       tc::fence_before_sync();
       __syncthreads();
 
-      // ---- O += P V (M = 128 rows, N = D, K = 128 keys; V MN-major)
+      // ---- O += P V (M = 128 rows, N = D, K = 128 keys; P from TMEM, V
+      // MN-major)
       if (tid == 0) {
         tc::fence_after_sync();
         const uint32_t ida = tc::idesc_f16(kRowsPerTile, D, true);
-        const uint32_t pa = smem_u32(sK), va = smem_u32(sV);
+        const uint32_t va = smem_u32(sV);
 #pragma unroll 1
         for (int kk = 0; kk < kChunk / 16; ++kk) {
-          const uint32_t offa = static_cast<uint32_t>((kk >> 2) * kRowsPerTile * 128 + (kk & 3) * 32);
           const uint32_t offv = static_cast<uint32_t>(kk * 16 * 128);
-          tc::mma_f16(t_o, tc::smem_desc_sw128(pa + offa, 1024),
-                      tc::smem_desc_sw128_mn(va + offv, kChunk * 128, 1024), ida,
-                      (o_valid || kk > 0) ? 1u : 0u);
+          tc::mma_f16_ts(t_o, t_sb + static_cast<uint32_t>(kk * 8),
+                         tc::smem_desc_sw128_mn(va + offv, kChunk * 128, 1024), ida,
+                         (o_valid || kk > 0) ? 1u : 0u);
         }
         tc::commit(bar_mma);
+        ++pv_pend;
       }
-
-      if (!cta_wait(bar_mma, ph_mma, &s_ok, p.status)) { alive = false; break; }
-      ph_mma ^= 1u;
-      o_valid = true;
-      tc::fence_after_sync();
+      auto pv_wait = [&]() -> bool {
+        if (!cta_wait(bar_mma, ph_pv, &s_ok, p.status)) return false;
+        ph_pv ^= 1u;
+        pv_pend = 0;
+        o_valid = true;
+        tc::fence_after_sync();
+        return true;
+      };
+      if (i + 1 < n_it) {
+        // The next chunk, by the workers (warps 1..) while warp 0 issues:
+        // K^ under P V(i) (P is in TMEM, sK is free), handed to warp 0 for
+        // its S; V^ once P V(i) has read sV. Warp 0's MMA issue may block
+        // while the tensor pipe is busy; the workers do not wait for it.
+        const int cn = chunk_of(i + 1);
+        const int jn = lo_min + cn * kChunk;
+        const int nn = min(kChunk, C - jn);
+        if (tid == 32) s_wok = 1;
+        if (warp == 0) {
+          __syncwarp();
+          named_sync(2, kStepThreads);              // K^ written (or a wait gave up)
+          if (tid == 0 && s_wok) issue_s(t_sbuf(i + 1));
+          __syncwarp();
+        } else {
+          const int wi = tid - 32;
+          bool ok = true;
+          if constexpr (!kQ4) {
+            f16_copy(0, jn, nn, wi, kWorkers);
+          } else {
+            if constexpr (L::kBulk) ok = worker_wait(bar_kv, ph_kv);
+            if (ok) {
+              uint32_t wk[9], wk2[9];
+              q4_load(wi, 0, L::kBulk ? sK + L::kRawK2 : nullptr, jn, nn, wk);
+              q4_load(wi + kWorkers, 0, L::kBulk ? sK + L::kRawK2 : nullptr, jn, nn, wk2);
+              if constexpr (L::kBulk) named_sync(1, kWorkers);   // raw K (in sK) consumed
+              q4_store(wi, 0, wk);
+              q4_store(wi + kWorkers, 0, wk2);
+            }
+          }
+          fence_proxy_async_smem();
+          named_arrive(2, kStepThreads);
+          if (ok) ok = worker_wait(bar_mma, ph_pv);
+          if (ok) {
+            if constexpr (!kQ4) {
+              f16_copy(1, jn, nn, wi, kWorkers);
+            } else {
+              uint32_t wv[9], wv2[9];
+              q4_load(wi, 1, L::kBulk ? smem + L::kRawV2 : nullptr, jn, nn, wv);
+              q4_load(wi + kWorkers, 1, L::kBulk ? smem + L::kRawV2 : nullptr, jn, nn, wv2);
+              q4_store(wi, 1, wv);
+              q4_store(wi + kWorkers, 1, wv2);
+            }
+            fence_proxy_async_smem();
+          }
+        }
+        __syncthreads();                            // V^ written, S issued
+        if (!s_wok) { alive = false; break; }
+        if constexpr (kQ4 && L::kBulk) {
+          ph_kv ^= 1u;
+          kv_pending = 0;
+        }
+        ph_pv ^= 1u;                                // P V(i) is done
+        pv_pend = 0;
+        o_valid = true;
+        tc::fence_after_sync();
+      } else {
+        if (!pv_wait()) { alive = false; break; }
+      }
+    }
+    // a unit that gave up waits (bounded) for its copies and MMAs still in
+    // flight before its smem and TMEM are reused or released
+    if (!alive && tid == 0) {
+      if (kv_pending > 0) mbar_wait_bounded(bar_kv, ph_kv);
+      if (pv_pend > 0) mbar_wait_bounded(bar_mma, ph_pv);
+      if (s_pend > 0) mbar_wait_bounded(bar_s, ph_s);
     }
 
     // ---- epilogue: normalised O rows from TMEM (each thread's columns in
