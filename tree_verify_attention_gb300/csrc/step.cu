@@ -1143,11 +1143,17 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
           // visible keys of this row form the range [kmin, kmax)
           const int kmin = min(max(lo - j0, 0), kChunk) - kb0;
           const int kmax = (node >= 0 ? nk : 0) - kb0;
+          if (kmin <= 0 && kmax >= 32) {
+            // every key of this thread's slice is visible (no range test)
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const float x = (k >= kmin && k < kmax) ? s[k] * sc : -INFINITY;
-            s[k] = x;
-            cm[k & 3] = fmaxf(cm[k & 3], x);
+            for (int k = 0; k < 32; ++k) cm[k & 3] = fmaxf(cm[k & 3], s[k]);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const float x = (k >= kmin && k < kmax) ? s[k] : -INFINITY;
+              s[k] = x;
+              cm[k & 3] = fmaxf(cm[k & 3], x);
+            }
           }
         } else {
           // tree keys t = 0..N-1 (N <= 65 < 128: one tree chunk); this
@@ -1155,7 +1161,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
           const uint32_t w = (node >= 0 && hc < kMaskWords) ? s_anc[node][hc] : 0u;
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
-            const float x = ((w >> k) & 1u) ? s[k] * sc : -INFINITY;
+            const float x = ((w >> k) & 1u) ? s[k] : -INFINITY;
             s[k] = x;
             cm[k & 3] = fmaxf(cm[k & 3], x);
           }
@@ -1163,7 +1169,9 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         s_pmax[hc][r] = fmaxf(fmaxf(cm[0], cm[1]), fmaxf(cm[2], cm[3]));
         __syncthreads();
         if (live) {
-          const float cmax = fmaxf(fmaxf(s_pmax[0][r], s_pmax[1][r]), fmaxf(s_pmax[2][r], s_pmax[3][r]));
+          // the scale (> 0) is applied to the row max and inside the exp:
+          // max(s) * sc is the max of the scaled scores
+          const float cmax = fmaxf(fmaxf(s_pmax[0][r], s_pmax[1][r]), fmaxf(s_pmax[2][r], s_pmax[3][r])) * sc;
           float alpha = 1.f;
           bool rescale = false;
           if (m_run == -INFINITY) {
@@ -1180,8 +1188,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
           uint32_t pw[16];
 #pragma unroll
           for (int k2 = 0; k2 < 16; ++k2) {
-            const float p0 = tc::ex2(s[2 * k2] - sub);
-            const float p1 = tc::ex2(s[2 * k2 + 1] - sub);
+            const float p0 = tc::ex2(fmaf(s[2 * k2], sc, -sub));
+            const float p1 = tc::ex2(fmaf(s[2 * k2 + 1], sc, -sub));
             rs4[k2 & 3] += p0 + p1;
             pw[k2] = pack_half2(p0, p1);
           }
@@ -1386,7 +1394,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
   // group's partials to be marked ready, then merges its share of the
   // group's rows over the splits by log-sum-exp: the rows (values, max and
   // sum) of every split's partial arrive by one bulk copy per split into
-  // smem; one warp per row turns the (max, sum) pairs into weights.
+  // smem, where each thread merges four columns of one row.
   if (unit >= 0 && p.splits > 1) {
     constexpr int RB = kPartRowBytes<D>;
     const int gi = unit / p.splits, split_ = unit % p.splits;
@@ -1416,55 +1424,38 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       if (tid == 0) report(p.status, DFV_DEV_TIMEOUT);
       return;
     }
-    float* s_w = reinterpret_cast<float*>(sQ);      // [nr][S] normalised weights
-#pragma unroll 1
-    for (int rr = warp; rr < nr; rr += kStepThreads / 32) {
-      auto ml = [&](int sp) { return *reinterpret_cast<const float2*>(mst + (static_cast<size_t>(sp) * nr + rr) * RB + D * 2); };
-      float M = -INFINITY;
-      for (int sp = lane; sp < S; sp += 32) M = fmaxf(M, ml(sp).x);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      float lsum = 0.f;
-      for (int sp = lane; sp < S; sp += 32) {
-        const float2 v = ml(sp);
-        const float w = v.x == -INFINITY ? 0.f : tc::ex2(v.x - M) * v.y;
-        s_w[rr * S + sp] = w;
-        lsum += w;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-      for (int sp = lane; sp < S; sp += 32) s_w[rr * S + sp] *= inv;
-      if (lane == 0 && p.lse != nullptr) {
-        const int rg = g_ * kRowsPerTile + r0 + rr;
-        const int node = div_small(rg, p.group_m), qh = h_ * p.group + rg - node * p.group;
-        p.lse[node * p.hq + qh] = (M + log2f(lsum)) * 0.69314718055994531f;
-      }
-    }
-    __syncthreads();
-    constexpr int PR = D / 8;
+    // Each thread merges four columns of one row over the splits; every
+    // thread of a row derives the row's weights from the staged (max, sum)
+    // tails itself, so no phase or barrier separates weights and sums.
+    constexpr int PR = D / 4;                       // four-column pieces per row
 #pragma unroll 1
     for (int it = tid; it < nr * PR; it += kStepThreads) {
       const int rr = it / PR, c = it % PR;
-      const float* w = s_w + rr * S;
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      const uint8_t* row0 = mst + static_cast<size_t>(rr) * RB;
+      const size_t sstride = static_cast<size_t>(nr) * RB;   // bytes between splits' rows
+      float M = -INFINITY;
+#pragma unroll 4
+      for (int sp = 0; sp < S; ++sp) M = fmaxf(M, reinterpret_cast<const float2*>(row0 + sp * sstride + D * 2)->x);
+      float lsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 2
       for (int sp = 0; sp < S; ++sp) {
-        const uint4 v = *reinterpret_cast<const uint4*>(mst + (static_cast<size_t>(sp) * nr + rr) * RB + c * 16);
-        const float wt = w[sp];
-        const __half2* hv = reinterpret_cast<const __half2*>(&v);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __half22float2(hv[e]);
-          acc[2 * e] += wt * f.x;
-          acc[2 * e + 1] += wt * f.y;
-        }
+        const float2 t = *reinterpret_cast<const float2*>(row0 + sp * sstride + D * 2);
+        const float w = t.x == -INFINITY ? 0.f : tc::ex2(t.x - M) * t.y;
+        lsum += w;
+        const uint2 v = *reinterpret_cast<const uint2*>(row0 + sp * sstride + c * 8);
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+        acc[0] += w * f0.x;
+        acc[1] += w * f0.y;
+        acc[2] += w * f1.x;
+        acc[3] += w * f1.y;
       }
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
       const int rg = g_ * kRowsPerTile + r0 + rr;
       const int node = div_small(rg, p.group_m), qh = h_ * p.group + rg - node * p.group;
-      float4* dst = reinterpret_cast<float4*>(p.out + (static_cast<size_t>(node) * p.hq + qh) * D + c * 8);
-      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(node) * p.hq + qh) * D + c * 4) =
+          make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+      if (c == 0 && p.lse != nullptr) p.lse[node * p.hq + qh] = (M + log2f(lsum)) * 0.69314718055994531f;
     }
   }
 }
