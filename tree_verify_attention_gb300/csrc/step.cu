@@ -834,7 +834,10 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     derive();
   }
   // ---- Q: once the bf16 rows have landed, warps 1..15 convert them into
-  // the fp16 swizzled tile in sQ; rows past the tile's are zero
+  // the fp16 swizzled tile in sQ; rows past the tile's are zero. No barrier
+  // of its own: the staged rows (in sK) are read before the barrier that
+  // precedes the first write into sK (the first chunk's K / V wait, or the
+  // one before a chunk built otherwise), and sQ before the one before S.
   if (unit >= 0 && li >= 0) {
     if (!wait_bounded([&]() { return mbar_try_wait(bar_q, 0); }) && li == 0)
       report(p.status, DFV_DEV_TIMEOUT);
@@ -848,7 +851,6 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       *reinterpret_cast<uint4*>(sQ + tc::sw128_offset(row, c, kRowsPerTile)) = v;
     }
   }
-  __syncthreads();   // Q converted, tree bookkeeping done
 
   // ---- logits: CTAs without an attention unit scan their staged slices;
   // when nothing is staged, every CTA scans slices with plain loads
@@ -1028,19 +1030,21 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       const int j0 = lo_min + cc * kChunk;
       const int nk = committed ? min(kChunk, C - j0) : 0;
       if (committed && !kQ4) {
+        __syncthreads();   // the staged Q rows (in sK) are converted
         f16_copy(0, j0, nk, tid, kStepThreads);
         f16_copy(1, j0, nk, tid, kStepThreads);
       } else if (committed) {
-        if constexpr (L::kBulk) alive = kv_wait();
+        if constexpr (L::kBulk) alive = kv_wait();   // (also: the staged Q rows are converted)
         if (alive) {
           uint32_t wk[9], wv[9];
           q4_load(tid, 0, L::kBulk ? sV + L::kRawK : nullptr, j0, nk, wk);
           q4_load(tid, 1, L::kBulk ? sV + L::kRawV : nullptr, j0, nk, wv);
-          if constexpr (L::kBulk) __syncthreads();   // raw rows (in sV) consumed
+          __syncthreads();   // raw rows (in sV) consumed; the staged Q rows converted
           q4_store(tid, 0, wk);
           q4_store(tid, 1, wv);
         }
       } else {
+        __syncthreads();   // the staged Q rows (in sK) are converted
         // tree chunk: keys t = 0..N-1 from tree_k / tree_v (bf16 -> fp16);
         // the other key rows are zero. The first TP pieces of each loader
         // thread were loaded at entry.
