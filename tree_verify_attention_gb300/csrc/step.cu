@@ -924,6 +924,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     bool o_valid = false, alive = true;
     const float sc = p.scale_log2;
     const int n_it = c1 - c0;
+    bool last_seen = true;         // this thread saw the last chunk's P V done
     auto chunk_of = [&](int i) { return i < n_tree ? T - 1 : c0 + (i - n_tree); };
     // S of chunk i in TMEM columns [0, 128) or [384, 512) by parity (clear
     // of O); its P (fp16 pairs) overwrites the first 64 of them
@@ -997,12 +998,6 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       named_sync(1, kWorkers);
       return s_wok != 0;
     };
-    auto kv_wait = [&]() -> bool {
-      if (!cta_wait(bar_kv, ph_kv, &s_ok, p.status)) return false;
-      ph_kv ^= 1u;
-      kv_pending = 0;
-      return true;
-    };
     // S = Q K^T (M = 128 rows, N = 128 keys, K = D) into t_dst. The issue
     // loop is unrolled and each descriptor is the tile's first plus the
     // step's offset (16-byte units): a rolled loop that rebuilt them cost
@@ -1034,14 +1029,24 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         f16_copy(0, j0, nk, tid, kStepThreads);
         f16_copy(1, j0, nk, tid, kStepThreads);
       } else if (committed) {
-        if constexpr (L::kBulk) alive = kv_wait();   // (also: the staged Q rows are converted)
+        // every thread waits for the raw rows itself; the barrier after the
+        // loads (raw rows consumed, staged Q rows converted) also makes the
+        // outcome of the wait the same for all
+        bool seen = true;
+        if constexpr (L::kBulk) seen = mbar_wait_bounded(bar_kv, ph_kv);
+        uint32_t wk[9], wv[9];
+        q4_load(tid, 0, L::kBulk ? sV + L::kRawK : nullptr, j0, nk, wk);
+        q4_load(tid, 1, L::kBulk ? sV + L::kRawV : nullptr, j0, nk, wv);
+        alive = __syncthreads_and(seen) != 0;
         if (alive) {
-          uint32_t wk[9], wv[9];
-          q4_load(tid, 0, L::kBulk ? sV + L::kRawK : nullptr, j0, nk, wk);
-          q4_load(tid, 1, L::kBulk ? sV + L::kRawV : nullptr, j0, nk, wv);
-          __syncthreads();   // raw rows (in sV) consumed; the staged Q rows converted
+          if constexpr (L::kBulk) {
+            ph_kv ^= 1u;
+            kv_pending = 0;
+          }
           q4_store(tid, 0, wk);
           q4_store(tid, 1, wv);
+        } else if (tid == 0) {
+          report(p.status, DFV_DEV_TIMEOUT);
         }
       } else {
         __syncthreads();   // the staged Q rows (in sK) are converted
@@ -1125,14 +1130,14 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       const int j0 = lo_min + cc * kChunk;
       const int nk = committed ? min(kChunk, C - j0) : 0;
       const uint32_t t_sb = t_sbuf(i);
-      if (!cta_wait(bar_s, ph_s, &s_ok, p.status)) { alive = false; break; }
-      ph_s ^= 1u;
-      s_pend = 0;
+      // every thread waits for S itself; the row-max barrier below makes
+      // the outcome the same for all
+      const bool s_seen = mbar_wait_bounded(bar_s, ph_s);
       tc::fence_after_sync();
       // K^ is consumed: the next chunk's raw K / V go in flight (every chunk
       // after the first is committed)
       if constexpr (L::kBulk && kQ4) {
-        if (tid == 0 && i + 1 < n_it) issue_kv(chunk_of(i + 1), sK + L::kRawK2, smem + L::kRawV2);
+        if (tid == 0 && s_seen && i + 1 < n_it) issue_kv(chunk_of(i + 1), sK + L::kRawK2, smem + L::kRawV2);
       }
 
       // ---- masked softmax of the 128-row tile: four threads per row, 32
@@ -1171,8 +1176,14 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
           }
         }
         s_pmax[hc][r] = fmaxf(fmaxf(cm[0], cm[1]), fmaxf(cm[2], cm[3]));
-        __syncthreads();
-        if (live) {
+        if (!__syncthreads_and(s_seen)) {
+          if (tid == 0) report(p.status, DFV_DEV_TIMEOUT);
+          alive = false;
+        } else {
+          ph_s ^= 1u;
+          s_pend = 0;
+        }
+        if (alive && live) {
           // the scale (> 0) is applied to the row max and inside the exp:
           // max(s) * sc is the max of the scaled scores
           const float cmax = fmaxf(fmaxf(s_pmax[0][r], s_pmax[1][r]), fmaxf(s_pmax[2][r], s_pmax[3][r])) * sc;
@@ -1211,7 +1222,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
               tc::st8(t_o + lane_base + col, ov);
             }
           }
-        } else {
+        } else if (alive) {
           // rows past the last: zero P (their O rows reach no output)
           uint32_t pw[16];
 #pragma unroll
@@ -1219,6 +1230,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
           tc::st16(t_sb + lane_base + hc * 16, pw);
         }
       }
+      if (!alive) break;   // S timed out (the same for every thread)
       tc::fence_before_sync();
       __syncthreads();
 
@@ -1236,14 +1248,6 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         tc::commit(bar_mma);
         ++pv_pend;
       }
-      auto pv_wait = [&]() -> bool {
-        if (!cta_wait(bar_mma, ph_pv, &s_ok, p.status)) return false;
-        ph_pv ^= 1u;
-        pv_pend = 0;
-        o_valid = true;
-        tc::fence_after_sync();
-        return true;
-      };
       if (i + 1 < n_it) {
         // The next chunk, by the workers (warps 1..) while warp 0 issues:
         // K^ under P V(i) (P is in TMEM, sK is free), handed to warp 0 for
@@ -1301,7 +1305,10 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         o_valid = true;
         tc::fence_after_sync();
       } else {
-        if (!pv_wait()) { alive = false; break; }
+        // the last chunk: every thread waits for P V itself; the
+        // epilogue's first barrier makes the outcome the same for all
+        last_seen = mbar_wait_bounded(bar_mma, ph_pv);
+        tc::fence_after_sync();
       }
     }
     // a unit that gave up waits (bounded) for its copies and MMAs still in
@@ -1318,7 +1325,20 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     // copy to the workspace; or straight to the output (fp32) when there is
     // one split
     s_l[hc][r] = l_half;
-    __syncthreads();
+    const bool pv_all = __syncthreads_and(last_seen) != 0;
+    if (n_it > 0 && alive) {
+      if (pv_all) {
+        ph_pv ^= 1u;
+        pv_pend = 0;
+        o_valid = true;
+      } else {
+        alive = false;
+        if (tid == 0) {
+          report(p.status, DFV_DEV_TIMEOUT);
+          mbar_wait_bounded(bar_mma, ph_pv);   // the MMAs still in flight (bounded)
+        }
+      }
+    }
     const bool ok_all = o_valid && alive;
     constexpr int RB = kPartRowBytes<D>;   // bytes of one partial row
     uint8_t* stage = smem;                 // [rows_g][RB], over sQ and sK (free after the last MMA)
