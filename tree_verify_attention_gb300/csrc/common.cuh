@@ -49,6 +49,20 @@ __device__ __forceinline__ void named_sync(int id, int count) {
 __device__ __forceinline__ void named_arrive(int id, int count) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// sync on named barrier `id` that also returns whether `v` held in every
+// one of the `count` threads.
+__device__ __forceinline__ bool named_sync_and(int id, int count, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
 
 __device__ __forceinline__ void report(uint32_t* status, uint32_t bits) {
   if (status != nullptr) atomicOr(status, bits);

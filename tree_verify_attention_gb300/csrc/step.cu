@@ -987,17 +987,9 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
           *reinterpret_cast<uint4*>(dst + tc::sw128_offset(key, pp * 8 + e, kChunk)) = o4[e];
       }
     };
-    // a wait of the workers alone: thread 32 polls, the workers meet
+    // the workers' K^ handed to warp 0: 0 when their wait for the raw rows
+    // gave up
     __shared__ int s_wok;
-    auto worker_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-      if (tid == 32) {
-        const bool ok = mbar_wait_bounded(bar, parity);
-        if (!ok) report(p.status, DFV_DEV_TIMEOUT);
-        s_wok = ok ? 1 : 0;
-      }
-      named_sync(1, kWorkers);
-      return s_wok != 0;
-    };
     // S = Q K^T (M = 128 rows, N = 128 keys, K = D) into t_dst. The issue
     // loop is unrolled and each descriptor is the tile's first plus the
     // step's offset (16-byte units): a rolled loop that rebuilt them cost
@@ -1256,31 +1248,41 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         const int cn = chunk_of(i + 1);
         const int jn = lo_min + cn * kChunk;
         const int nn = min(kChunk, C - jn);
-        if (tid == 32) s_wok = 1;
+        if (tid == 32) s_wok = 1;   // (the F16 and unstaged paths have no copy to wait on)
+        bool ok = true;             // a worker: every wait of this chunk ended in time
         if (warp == 0) {
           __syncwarp();
           named_sync(2, kStepThreads);              // K^ written (or a wait gave up)
           if (tid == 0 && s_wok) issue_s(t_sbuf(i + 1));
           __syncwarp();
         } else {
+          // every worker waits on the copy and on P V itself; the barriers
+          // that follow carry the outcome to all
           const int wi = tid - 32;
-          bool ok = true;
           if constexpr (!kQ4) {
             f16_copy(0, jn, nn, wi, kWorkers);
           } else {
-            if constexpr (L::kBulk) ok = worker_wait(bar_kv, ph_kv);
+            bool seen = true;
+            if constexpr (L::kBulk) seen = mbar_wait_bounded(bar_kv, ph_kv);
+            uint32_t wk[9], wk2[9];
+            q4_load(wi, 0, L::kBulk ? sK + L::kRawK2 : nullptr, jn, nn, wk);
+            q4_load(wi + kWorkers, 0, L::kBulk ? sK + L::kRawK2 : nullptr, jn, nn, wk2);
+            if constexpr (L::kBulk) {
+              ok = named_sync_and(1, kWorkers, seen);   // raw K (in sK) consumed
+              if (!ok && tid == 32) report(p.status, DFV_DEV_TIMEOUT);
+            }
+            if (tid == 32) s_wok = ok ? 1 : 0;
             if (ok) {
-              uint32_t wk[9], wk2[9];
-              q4_load(wi, 0, L::kBulk ? sK + L::kRawK2 : nullptr, jn, nn, wk);
-              q4_load(wi + kWorkers, 0, L::kBulk ? sK + L::kRawK2 : nullptr, jn, nn, wk2);
-              if constexpr (L::kBulk) named_sync(1, kWorkers);   // raw K (in sK) consumed
               q4_store(wi, 0, wk);
               q4_store(wi + kWorkers, 0, wk2);
             }
           }
           fence_proxy_async_smem();
           named_arrive(2, kStepThreads);
-          if (ok) ok = worker_wait(bar_mma, ph_pv);
+          if (ok) {
+            ok = mbar_wait_bounded(bar_mma, ph_pv);
+            if (!ok) report(p.status, DFV_DEV_TIMEOUT);
+          }
           if (ok) {
             if constexpr (!kQ4) {
               f16_copy(1, jn, nn, wi, kWorkers);
@@ -1294,8 +1296,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
             fence_proxy_async_smem();
           }
         }
-        __syncthreads();                            // V^ written, S issued
-        if (!s_wok) { alive = false; break; }
+        // V^ written, S issued; false if any wait gave up
+        if (!__syncthreads_and(warp == 0 || ok)) { alive = false; break; }
         if constexpr (kQ4 && L::kBulk) {
           ph_kv ^= 1u;
           kv_pending = 0;
@@ -1422,14 +1424,6 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
   if (unit >= 0 && p.splits > 1) {
     constexpr int RB = kPartRowBytes<D>;
     const int gi = unit / p.splits, split_ = unit % p.splits;
-    if (warp == 0) {
-      __syncwarp();   // s_tag was written by lane 0
-      const bool ok = wait_ready(p.ready + static_cast<size_t>(gi) * p.splits, p.splits, s_tag);
-      if (!ok && lane == 0) report(p.status, DFV_DEV_TIMEOUT);
-      if (lane == 0) s_ok = ok ? 1 : 0;
-    }
-    __syncthreads();
-    if (!s_ok) return;
     const int h_ = gi / p.n_grp, g_ = gi % p.n_grp;
     const int rows_t = min(kRowsPerTile, p.rows - g_ * kRowsPerTile);
     const int r0 = split_ * rows_t / p.splits, r1 = (split_ + 1) * rows_t / p.splits;
@@ -1437,15 +1431,29 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     if (nr <= 0) return;
     const size_t ubase = static_cast<size_t>(gi) * S;
     uint8_t* mst = sK;   // [S][nr][RB]
-    if (tid == 0) {
-      fence_proxy_async_global();   // the acquired partials, before the async-proxy reads
-      mbar_arrive_expect_tx(bar_q, static_cast<uint32_t>(S * nr * RB));
-      for (int s = 0; s < S; ++s)
-        bulk_g2s(mst + static_cast<size_t>(s) * nr * RB, p.part + ((ubase + s) * kRowsPerTile + r0) * RB,
-                 static_cast<uint32_t>(nr * RB), bar_q);
+    if (blk == p.walker) __syncthreads();   // (a walker with a unit: its copies out of sK are done)
+    // Warp 0 waits for the group's ready words and lane 0 then starts the
+    // copies; the other threads only wait for the copies to land (no CTA
+    // barrier between). If the ready wait gives up, no copy starts and
+    // every thread's own wait runs out and returns.
+    if (warp == 0) {
+      __syncwarp();   // s_tag was written by lane 0
+      const bool ok = wait_ready(p.ready + static_cast<size_t>(gi) * p.splits, p.splits, s_tag);
+      if (lane == 0) {
+        if (ok) {
+          fence_proxy_async_global();   // the acquired partials, before the async-proxy reads
+          mbar_arrive_expect_tx(bar_q, static_cast<uint32_t>(S * nr * RB));
+          for (int s = 0; s < S; ++s)
+            bulk_g2s(mst + static_cast<size_t>(s) * nr * RB, p.part + ((ubase + s) * kRowsPerTile + r0) * RB,
+                     static_cast<uint32_t>(nr * RB), bar_q);
+        } else {
+          report(p.status, DFV_DEV_TIMEOUT);
+        }
+      }
+      if (!ok) return;
     }
     if (!wait_bounded([&]() { return mbar_try_wait(bar_q, 1); })) {
-      if (tid == 0) report(p.status, DFV_DEV_TIMEOUT);
+      if (tid == 32) report(p.status, DFV_DEV_TIMEOUT);
       return;
     }
     // Each thread merges four columns of one row over the splits; every
