@@ -925,6 +925,13 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     const float sc = p.scale_log2;
     const int n_it = c1 - c0;
     bool last_seen = true;         // this thread saw the last chunk's P V done
+    // Hand-off to warp 0 (named barrier 3): warp 0 waits until every thread
+    // has arrived, the others arrive and go on. Two uses are always
+    // separated by a full CTA barrier.
+    auto to_warp0 = [&]() {
+      if (warp == 0) named_sync(3, kStepThreads);
+      else named_arrive(3, kStepThreads);
+    };
     auto chunk_of = [&](int i) { return i < n_tree ? T - 1 : c0 + (i - n_tree); };
     // S of chunk i in TMEM columns [0, 128) or [384, 512) by parity (clear
     // of O); its P (fp16 pairs) overwrites the first 64 of them
@@ -1107,7 +1114,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         }
       }
       fence_proxy_async_smem();
-      __syncthreads();
+      to_warp0();   // K^ and V^ written: warp 0 issues S, the others go on to wait for it
       if (alive && tid == 0) issue_s(t_sbuf(0));
     }
 
@@ -1224,7 +1231,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
       }
       if (!alive) break;   // S timed out (the same for every thread)
       tc::fence_before_sync();
-      __syncthreads();
+      to_warp0();   // P written: warp 0 issues P V, the others go on
 
       // ---- O += P V (M = 128 rows, N = D, K = 128 keys; P from TMEM, V
       // MN-major)
@@ -1380,7 +1387,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
     }
     tc::fence_before_sync();
     fence_proxy_async_smem();   // the staged rows, before the bulk copy reads them
-    __syncthreads();
+    to_warp0();   // warp 0 copies the partials out and frees TMEM; the others go on
     if (p.splits > 1) {
       uint8_t* part = p.part + static_cast<size_t>(unit) * kRowsPerTile * RB;
       if (!ok_all) {
