@@ -163,6 +163,14 @@ def test_f16_attention_context_and_window_edges(C, window):
     _attn_case(cfg, C, window, fmt="f16", seed=C + window)
 
 
+@pytest.mark.parametrize("D,hq,hkv", [(64, 16, 4), (128, 16, 4), (256, 8, 2)])
+def test_f16_attention_multi_chunk_units(D, hq, hkv):
+    """F16 rows through the pipelined chunk loop: units of several 128-key
+    chunks each (see test_gpu_kernels.test_attention_multi_chunk_units)."""
+    cfg = replace(W.SHORT, n_q_heads=hq, n_kv_heads=hkv, head_dim=D)
+    _attn_case(cfg, 16000, 0, fmt="f16", seed=D + 1)
+
+
 @pytest.mark.parametrize("D,hq,hkv", [(64, 4, 1), (128, 8, 2), (128, 32, 4)])
 def test_f16_attention_head_dims(D, hq, hkv):
     cfg = replace(W.TINY, head_dim=D, n_q_heads=hq, n_kv_heads=hkv)

@@ -291,6 +291,20 @@ def test_attention_head_dims_and_groups(D, hq, hkv):
     _attn_case(cfg, 700, 300)
 
 
+@pytest.mark.parametrize("D,hq,hkv", [(64, 16, 4), (128, 16, 4), (256, 8, 2)])
+@pytest.mark.parametrize("window", [0, 5000])
+def test_attention_multi_chunk_units(D, hq, hkv, window):
+    """Contexts long enough that the attention units take several 128-key
+    chunks each (the pipelined chunk loop: the next chunk's rows read and
+    decoded while the current one's P V runs): 4 KV heads x 1 row tile x
+    126 chunks cannot give every split one chunk on any GPU of up to 256
+    SMs. At head dims 64 and 128 the Q4_0 rows are read from the cache
+    directly, at 256 through the staged copies."""
+    from dataclasses import replace
+    cfg = replace(W.SHORT, n_q_heads=hq, n_kv_heads=hkv, head_dim=D)
+    _attn_case(cfg, 16000, window, seed=D + window)
+
+
 @pytest.mark.parametrize("budget", [0, 8, 22, 48, 64])
 @pytest.mark.parametrize("shape", ["chain", "kary4", "random"])
 def test_attention_sweep_shapes(budget, shape):

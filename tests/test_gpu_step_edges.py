@@ -40,6 +40,20 @@ def test_step_head_dims_chained(D, hq, hkv, window):
     r.check_cache()
 
 
+@pytest.mark.parametrize("D,hq,hkv", [(64, 16, 4), (128, 16, 4)])
+def test_step_multi_chunk_units_chained(D, hq, hkv):
+    """Three chained whole steps at a context where the attention units
+    take several key chunks each, at head dims whose Q4_0 rows are read
+    from the cache directly: every output and committed byte against the
+    oracle."""
+    cfg = replace(W.SHORT, name=f"mc_d{D}_h{hq}x{hkv}", ctx_len=16000, window=0,
+                  n_q_heads=hq, n_kv_heads=hkv, head_dim=D, vocab=5000)
+    r = Run(cfg, cfg.ctx_len + 4 * cfg.n_nodes)
+    lens = [r.run(W.make_step(cfg, s)) for s in range(3)]
+    assert max(lens) > 1
+    r.check_cache()
+
+
 class EmptyRun(Run):
     """A sequence whose cache starts empty (ctx_len = 0)."""
 
