@@ -58,6 +58,9 @@ static void check(int N, int hq, int hkv, int D, int W, int cap, int V, int dt, 
   CHECK(pl.splits >= 1 && pl.units == hkv * pl.n_grp * pl.splits && pl.units <= pl.grid,
         "%s units %d splits %d", tag, pl.units, pl.splits);
   CHECK(pl.walker == (pl.grid > pl.units ? pl.grid - 1 : 0), "%s walker %d", tag, pl.walker);
+  // the walker holds no attention unit (its merge would otherwise need a
+  // barrier after the walk before its copies into sK)
+  CHECK(pl.walker >= pl.units, "%s the walker %d holds an attention unit", tag, pl.walker);
   // the walker stages every argmax partial in its Q tile
   CHECK(static_cast<long>(pl.lunits) * static_cast<long>(sizeof(dfv::ArgPartial)) <= tile,
         "%s lunits %d exceed the walker's staging", tag, pl.lunits);
@@ -97,19 +100,6 @@ static void check(int N, int hq, int hkv, int D, int W, int cap, int V, int dt, 
     for (int u = 0; u < pl.lunits; ++u) CHECK(seen[u] == 1, "%s slice %d held %d times", tag, u, seen[u]);
   } else {
     for (int b = 0; b < pl.grid; ++b) CHECK(pl.lslot[b] == 0, "%s CTA %d stages without bulk", tag, b);
-  }
-  // the split merge stages (max, sum) pairs and weights of its rows in the Q tile
-  if (pl.splits > 1) {
-    int worst = 0;
-    for (int g = 0; g < pl.n_grp; ++g) {
-      const int a_rows = pl.rows - g * 128 < 128 ? pl.rows - g * 128 : 128;
-      const int rows_t = a_rows;
-      for (int sp = 0; sp < pl.splits; ++sp) {
-        const int nr = (sp + 1) * rows_t / pl.splits - sp * rows_t / pl.splits;
-        if (nr * pl.splits > worst) worst = nr * pl.splits;
-      }
-    }
-    CHECK(worst * 12 <= tile, "%s merge staging %d bytes", tag, worst * 12);
   }
   // workspace regions in order, 256-byte aligned
   const size_t groups = static_cast<size_t>(hkv) * pl.n_grp;
