@@ -6,11 +6,10 @@ devices of 100 to 300 SMs (the grid is capped at 256 CTAs).
 Checked there: the 128-row tiles cover every row, every logits slice is
 staged by exactly one CTA (a CTA without a unit, or a unit of a tile of at
 most 32 rows, which stages one round in the smem its tile leaves free), a
-round of staged slices fits half of a staging area, bulk-copied slices stay 16-byte
-aligned, the argmax partials fit the walker's Q tile, the walker holds no
-attention unit, the split merge's
-staging fits, and the workspace regions are ordered, aligned and large
-enough."""
+round of staged slices fits half of a staging area, bulk-copied slices
+stay 16-byte aligned, the argmax partials fit the walker's Q tile, the
+walker holds no attention unit, the split merge's staging fits, and the
+workspace regions are ordered, aligned and large enough."""
 
 import os
 import shutil
